@@ -1,0 +1,494 @@
+/*
+ * uzip oracle -- plain single-threaded C implementation of the container.
+ *
+ * TEST INFRASTRUCTURE ONLY: called by the tests, the smoke check and the
+ * benchmark's CPU-baseline leg, never by the library.  It is written for
+ * reading, not for speed: every step runs in the order the format states,
+ * with plain integer division, and no blocking, vectorisation or fusion.
+ *
+ * Sources for each step (the pages, then the format readings R1..R20 of the
+ * design notes where the pages are silent):
+ *   split / merge ........ UCCL-Zip Fig. 2 caption (exponent field vs sign and
+ *                          fraction); R1 byte layout of the remainder.
+ *   local tables ......... UCCL-Zip Fig. 5 caption (each block builds its own
+ *                          table); R3 chunking, R4 histogram, R5 normalisation.
+ *   entropy coder ........ UCCL-Zip Fig. 2 caption ("ANS"); R6 rANS constants,
+ *                          R7 lane interleaving and word order, R8 stream.
+ *   RAW fallback ......... NCCLZ Sec. IV-B and IV-C, Alg. 1 (store RAW when
+ *                          coding does not pay); R9 threshold.
+ *   frame header ......... NCCLZ Sec. IV-B and IV-D2 (self-describing header
+ *                          plus payload); R10 padding, R11 header fields.
+ *   receiver validation .. NCCLZ Alg. 2 (validate before use); R12 checks.
+ */
+#include "uzip_oracle.h"
+
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* little-endian helpers (the container is little endian on every host)     */
+
+static uint64_t rd_le(const uint8_t* p, int nbytes) {
+    uint64_t v = 0;
+    for (int i = nbytes - 1; i >= 0; --i) v = (v << 8) | p[i];
+    return v;
+}
+
+static void wr_le(uint8_t* p, uint64_t v, int nbytes) {
+    for (int i = 0; i < nbytes; ++i) {
+        p[i] = (uint8_t)(v & 0xFF);
+        v >>= 8;
+    }
+}
+
+static uint64_t round16(uint64_t v) { return (v + 15u) / 16u * 16u; }
+
+static int remainder_bytes(int dtype) { return dtype == ORC_BF16 ? 1 : 3; }
+
+/* ------------------------------------------------------------------------ */
+/* R1: split each value into its exponent byte and its sign|fraction bits.  */
+/* bf16 = s | e(8) | m(7):  rem = s<<7 | m           (1 byte)              */
+/* fp32 = s | e(8) | m(23): rem = s<<23 | m          (3 bytes, LE)         */
+
+int orc_split(int dtype, const void* in, uint64_t n, uint8_t* exps, uint8_t* rem) {
+    const uint8_t* src = (const uint8_t*)in;
+    if (dtype == ORC_BF16) {
+        for (uint64_t i = 0; i < n; ++i) {
+            uint32_t bits = (uint32_t)rd_le(src + 2 * i, 2);
+            uint32_t sign = (bits >> 15) & 1u;
+            uint32_t e = (bits >> 7) & 0xFFu;
+            uint32_t m = bits & 0x7Fu;
+            exps[i] = (uint8_t)e;
+            rem[i] = (uint8_t)((sign << 7) | m);
+        }
+        return ORC_OK;
+    }
+    if (dtype == ORC_FP32) {
+        for (uint64_t i = 0; i < n; ++i) {
+            uint32_t bits = (uint32_t)rd_le(src + 4 * i, 4);
+            uint32_t sign = (bits >> 31) & 1u;
+            uint32_t e = (bits >> 23) & 0xFFu;
+            uint32_t m = bits & 0x7FFFFFu;
+            exps[i] = (uint8_t)e;
+            wr_le(rem + 3 * i, ((uint64_t)sign << 23) | m, 3);
+        }
+        return ORC_OK;
+    }
+    return ORC_ERR_UNSUPPORTED_DTYPE;
+}
+
+int orc_merge(int dtype, const uint8_t* exps, const uint8_t* rem, uint64_t n, void* out) {
+    uint8_t* dst = (uint8_t*)out;
+    if (dtype == ORC_BF16) {
+        for (uint64_t i = 0; i < n; ++i) {
+            uint32_t r = rem[i];
+            uint32_t sign = (r >> 7) & 1u;
+            uint32_t m = r & 0x7Fu;
+            uint32_t bits = (sign << 15) | ((uint32_t)exps[i] << 7) | m;
+            wr_le(dst + 2 * i, bits, 2);
+        }
+        return ORC_OK;
+    }
+    if (dtype == ORC_FP32) {
+        for (uint64_t i = 0; i < n; ++i) {
+            uint32_t r = (uint32_t)rd_le(rem + 3 * i, 3);
+            uint32_t sign = (r >> 23) & 1u;
+            uint32_t m = r & 0x7FFFFFu;
+            uint32_t bits = (sign << 31) | ((uint32_t)exps[i] << 23) | m;
+            wr_le(dst + 4 * i, bits, 4);
+        }
+        return ORC_OK;
+    }
+    return ORC_ERR_UNSUPPORTED_DTYPE;
+}
+
+/* ------------------------------------------------------------------------ */
+/* R4: 256-bin histogram of one chunk's exponent bytes.                     */
+
+void orc_histogram(const uint8_t* exps, uint32_t n_c, uint32_t counts[256]) {
+    for (int s = 0; s < 256; ++s) counts[s] = 0;
+    for (uint32_t i = 0; i < n_c; ++i) counts[exps[i]] += 1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* R5: deterministic largest-remainder normalisation to M = 4096.           */
+/*  1. f_s = floor(c_s*M/N), r_s = (c_s*M) mod N for each present s;        */
+/*     a present s with f_s = 0 is raised to 1 and marked boosted.          */
+/*  2. S = sum f.  If S < M: +1 to each of the first M-S non-boosted        */
+/*     present symbols ordered by (r_s descending, s ascending).            */
+/*  3. If S > M: S-M times, -1 to the symbol with the largest f (ties: the  */
+/*     smallest s).                                                         */
+
+int orc_normalise(const uint32_t counts[256], uint32_t n_c, uint16_t freq[256]) {
+    uint64_t total = 0;
+    for (int s = 0; s < 256; ++s) total += counts[s];
+    if (n_c == 0 || total != n_c) return ORC_ERR_INVALID_ARG;
+
+    uint32_t f[256];
+    uint64_t r[256];
+    int boosted[256];
+    for (int s = 0; s < 256; ++s) {
+        f[s] = 0;
+        r[s] = 0;
+        boosted[s] = 0;
+        if (counts[s] == 0) continue;
+        uint64_t scaled = (uint64_t)counts[s] * ORC_M;
+        f[s] = (uint32_t)(scaled / n_c);
+        r[s] = scaled % n_c;
+        if (f[s] == 0) {
+            f[s] = 1;
+            boosted[s] = 1;
+        }
+    }
+    uint32_t sum = 0;
+    for (int s = 0; s < 256; ++s) sum += f[s];
+
+    if (sum < ORC_M) {
+        int taken[256];
+        for (int s = 0; s < 256; ++s) taken[s] = 0;
+        uint32_t need = ORC_M - sum;
+        for (uint32_t k = 0; k < need; ++k) {
+            int best = -1;
+            for (int s = 0; s < 256; ++s) {
+                if (counts[s] == 0 || boosted[s] || taken[s]) continue;
+                if (best < 0 || r[s] > r[best]) best = s; /* ascending s keeps the first of ties */
+            }
+            if (best < 0) return ORC_ERR_INVALID_ARG; /* cannot happen: M-S < #non-boosted */
+            f[best] += 1;
+            taken[best] = 1;
+        }
+    } else if (sum > ORC_M) {
+        uint32_t excess = sum - ORC_M;
+        for (uint32_t k = 0; k < excess; ++k) {
+            int best = 0;
+            for (int s = 1; s < 256; ++s)
+                if (f[s] > f[best]) best = s;
+            f[best] -= 1; /* f[best] >= 2 here, since S > M >= 256 >= #present */
+        }
+    }
+    for (int s = 0; s < 256; ++s) freq[s] = (uint16_t)f[s];
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* R6/R7: interleaved rANS, 32 lanes, x in [2^16, 2^32), 16-bit words.      */
+/* Symbol i belongs to lane i mod 32 and to step i / 32.  The encoder runs  */
+/* steps from last to first; the stream lists, step by step from the first, */
+/* the words each step's renormalising lanes need, in ascending lane order. */
+
+static void cumulative(const uint16_t freq[256], uint32_t cum[257]) {
+    cum[0] = 0;
+    for (int s = 0; s < 256; ++s) cum[s + 1] = cum[s] + freq[s];
+}
+
+int orc_rans_encode(const uint8_t* syms, uint32_t n_c, const uint16_t freq[256],
+                    uint32_t states[32], uint16_t* words, uint32_t* n_words) {
+    uint32_t cum[257];
+    cumulative(freq, cum);
+    if (cum[256] != ORC_M) return ORC_ERR_INVALID_ARG;
+
+    uint8_t* emitted = (uint8_t*)calloc(n_c ? n_c : 1, 1);
+    uint16_t* word_of = (uint16_t*)calloc(n_c ? n_c : 1, sizeof(uint16_t));
+    if (!emitted || !word_of) {
+        free(emitted);
+        free(word_of);
+        return ORC_ERR_INVALID_ARG;
+    }
+    uint32_t x[32];
+    for (int j = 0; j < 32; ++j) x[j] = ORC_RANS_L;
+
+    uint32_t steps = (n_c + ORC_LANES - 1) / ORC_LANES;
+    int status = ORC_OK;
+    for (uint32_t t = steps; t-- > 0 && status == ORC_OK;) {
+        for (uint32_t j = 0; j < ORC_LANES; ++j) {
+            uint32_t i = t * ORC_LANES + j;
+            if (i >= n_c) continue;
+            uint32_t s = syms[i];
+            uint32_t f = freq[s];
+            if (f == 0) {
+                status = ORC_ERR_INVALID_ARG;
+                break;
+            }
+            uint64_t x_max = (uint64_t)f << (32 - ORC_PROB_BITS); /* f * 2^20 */
+            if ((uint64_t)x[j] >= x_max) {
+                word_of[i] = (uint16_t)(x[j] & 0xFFFFu);
+                emitted[i] = 1;
+                x[j] >>= 16;
+            }
+            x[j] = (x[j] / f) * ORC_M + (x[j] % f) + cum[s];
+        }
+    }
+    if (status == ORC_OK) {
+        uint32_t w = 0;
+        for (uint32_t i = 0; i < n_c; ++i)
+            if (emitted[i]) words[w++] = word_of[i];
+        *n_words = w;
+        for (int j = 0; j < 32; ++j) states[j] = x[j];
+    }
+    free(emitted);
+    free(word_of);
+    return status;
+}
+
+int orc_rans_decode(const uint32_t states_in[32], const uint16_t* words, uint32_t n_words,
+                    const uint16_t freq[256], uint32_t n_c, uint8_t* syms) {
+    uint32_t cum[257];
+    cumulative(freq, cum);
+    if (cum[256] != ORC_M) return ORC_ERR_CORRUPT;
+
+    /* slot -> symbol: slots [cum_s, cum_s + f_s) belong to s (R14) */
+    uint8_t sym_of_slot[ORC_M];
+    for (int s = 0; s < 256; ++s)
+        for (uint32_t k = cum[s]; k < cum[s + 1]; ++k) sym_of_slot[k] = (uint8_t)s;
+
+    uint32_t x[32];
+    for (int j = 0; j < 32; ++j) {
+        if (states_in[j] < ORC_RANS_L) return ORC_ERR_CORRUPT;
+        x[j] = states_in[j];
+    }
+    uint32_t pos = 0;
+    uint32_t steps = (n_c + ORC_LANES - 1) / ORC_LANES;
+    for (uint32_t t = 0; t < steps; ++t) {
+        for (uint32_t j = 0; j < ORC_LANES; ++j) {
+            uint32_t i = t * ORC_LANES + j;
+            if (i >= n_c) continue;
+            uint32_t slot = x[j] & (ORC_M - 1);
+            uint32_t s = sym_of_slot[slot];
+            x[j] = freq[s] * (x[j] >> ORC_PROB_BITS) + slot - cum[s];
+            if (x[j] < ORC_RANS_L) {
+                if (pos >= n_words) return ORC_ERR_CORRUPT;
+                x[j] = (x[j] << 16) | words[pos];
+                pos += 1;
+            }
+            syms[i] = (uint8_t)s;
+        }
+    }
+    for (int j = 0; j < 32; ++j)
+        if (x[j] != ORC_RANS_L) return ORC_ERR_CORRUPT;
+    if (pos != n_words) return ORC_ERR_CORRUPT;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* R8/R9: one chunk stream.                                                  */
+/*   coded: u32 state[32] | u8 bitmap[32] | u16 f[K] (present s ascending)   */
+/*          | u16 words[W];  len = 160 + 2K + 2W                             */
+/*   raw:   the n_c exponent bytes; len = n_c                                */
+/* Coded iff len_coded < n_c.                                                */
+
+int orc_encode_chunk(const uint8_t* exps, uint32_t n_c, int force_coded,
+                     uint8_t* out, uint32_t* len, int* raw) {
+    if (n_c == 0 || n_c > ORC_CHUNK_ELEMS) return ORC_ERR_INVALID_ARG;
+    uint32_t counts[256];
+    uint16_t freq[256];
+    orc_histogram(exps, n_c, counts);
+    int st = orc_normalise(counts, n_c, freq);
+    if (st != ORC_OK) return st;
+
+    uint32_t states[32];
+    uint32_t n_words = 0;
+    uint16_t* words = (uint16_t*)malloc((size_t)n_c * sizeof(uint16_t));
+    if (!words) return ORC_ERR_INVALID_ARG;
+    st = orc_rans_encode(exps, n_c, freq, states, words, &n_words);
+    if (st != ORC_OK) {
+        free(words);
+        return st;
+    }
+    uint32_t k = 0;
+    for (int s = 0; s < 256; ++s)
+        if (freq[s] > 0) k += 1;
+    uint64_t len_coded = 160u + 2u * (uint64_t)k + 2u * (uint64_t)n_words;
+
+    if (force_coded || len_coded < n_c) {
+        uint8_t* p = out;
+        for (int j = 0; j < 32; ++j) wr_le(p + 4 * j, states[j], 4);
+        p += 128;
+        memset(p, 0, 32);
+        for (int s = 0; s < 256; ++s)
+            if (freq[s] > 0) p[s >> 3] |= (uint8_t)(1u << (s & 7));
+        p += 32;
+        for (int s = 0; s < 256; ++s)
+            if (freq[s] > 0) {
+                wr_le(p, freq[s], 2);
+                p += 2;
+            }
+        for (uint32_t w = 0; w < n_words; ++w) {
+            wr_le(p, words[w], 2);
+            p += 2;
+        }
+        *len = (uint32_t)len_coded;
+        *raw = 0;
+    } else {
+        memcpy(out, exps, n_c);
+        *len = n_c;
+        *raw = 1;
+    }
+    free(words);
+    return ORC_OK;
+}
+
+int orc_decode_chunk(const uint8_t* stream, uint32_t len, int raw, uint32_t n_c, uint8_t* exps) {
+    if (n_c == 0 || n_c > ORC_CHUNK_ELEMS) return ORC_ERR_CORRUPT;
+    if (raw) {
+        if (len != n_c) return ORC_ERR_CORRUPT;
+        memcpy(exps, stream, n_c);
+        return ORC_OK;
+    }
+    if (len < 160) return ORC_ERR_CORRUPT;
+    uint32_t states[32];
+    for (int j = 0; j < 32; ++j) states[j] = (uint32_t)rd_le(stream + 4 * j, 4);
+    const uint8_t* bitmap = stream + 128;
+    uint16_t freq[256];
+    uint32_t k = 0;
+    for (int s = 0; s < 256; ++s) {
+        freq[s] = 0;
+        if (bitmap[s >> 3] & (1u << (s & 7))) k += 1;
+    }
+    if ((uint64_t)len < 160u + 2u * (uint64_t)k) return ORC_ERR_CORRUPT;
+    if ((len - 160u - 2u * k) % 2u != 0) return ORC_ERR_CORRUPT;
+    uint32_t n_words = (len - 160u - 2u * k) / 2u;
+    const uint8_t* fp = stream + 160;
+    uint32_t sum = 0;
+    for (int s = 0; s < 256; ++s) {
+        if (!(bitmap[s >> 3] & (1u << (s & 7)))) continue;
+        uint32_t f = (uint32_t)rd_le(fp, 2);
+        fp += 2;
+        if (f == 0 || f > ORC_M) return ORC_ERR_CORRUPT;
+        freq[s] = (uint16_t)f;
+        sum += f;
+    }
+    if (sum != ORC_M) return ORC_ERR_CORRUPT;
+    uint16_t* words = (uint16_t*)malloc((size_t)(n_words ? n_words : 1) * sizeof(uint16_t));
+    if (!words) return ORC_ERR_CORRUPT;
+    for (uint32_t w = 0; w < n_words; ++w) words[w] = (uint16_t)rd_le(fp + 2 * w, 2);
+    int st = orc_rans_decode(states, words, n_words, freq, n_c, exps);
+    free(words);
+    return st;
+}
+
+/* ------------------------------------------------------------------------ */
+/* R3/R10/R11: the container.                                                */
+/*   [0,64)         header: "UZP1" | u16 version=1 | u8 dtype | u8 flags=0 |  */
+/*                  u64 n | u32 chunk_elems | u32 C | u64 rem_offset |        */
+/*                  u64 exp_offset | u64 total_bytes | 16 zero bytes          */
+/*   [64,64+8C)     u64 offset of chunk c's stream from exp_offset            */
+/*   [64+8C,64+12C) u32 length of chunk c (bit 31 = RAW)                      */
+/*   rem_offset = round16(64+12C):      remainder plane, n*rb bytes           */
+/*   exp_offset = round16(rem_offset + n*rb): chunk streams, each padded to   */
+/*                16 bytes; every padding byte is zero.                       */
+
+static uint64_t num_chunks(uint64_t n) { return (n + ORC_CHUNK_ELEMS - 1) / ORC_CHUNK_ELEMS; }
+
+static uint32_t chunk_elems(uint64_t n, uint64_t c) {
+    uint64_t start = c * ORC_CHUNK_ELEMS;
+    uint64_t left = n - start;
+    return (uint32_t)(left < ORC_CHUNK_ELEMS ? left : ORC_CHUNK_ELEMS);
+}
+
+static uint64_t rem_offset_of(uint64_t n) { return round16(ORC_HEADER_BYTES + 12u * num_chunks(n)); }
+
+static uint64_t exp_offset_of(int dtype, uint64_t n) {
+    return round16(rem_offset_of(n) + n * (uint64_t)remainder_bytes(dtype));
+}
+
+uint64_t orc_container_bound(int dtype, uint64_t n) {
+    uint64_t bound = exp_offset_of(dtype, n);
+    uint64_t c_count = num_chunks(n);
+    for (uint64_t c = 0; c < c_count; ++c) bound += round16(chunk_elems(n, c));
+    return bound;
+}
+
+int orc_compress(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t cap,
+                 uint64_t* total) {
+    if (dtype != ORC_BF16 && dtype != ORC_FP32) return ORC_ERR_UNSUPPORTED_DTYPE;
+    if (num_chunks(n) > 0xFFFFFFFFull) return ORC_ERR_INVALID_ARG;
+    if ((n > 0 && in == NULL) || out == NULL) return ORC_ERR_INVALID_ARG;
+    uint64_t bound = orc_container_bound(dtype, n);
+    if (cap < bound) return ORC_ERR_CAPACITY;
+
+    uint64_t c_count = num_chunks(n);
+    uint64_t rem_offset = rem_offset_of(n);
+    uint64_t exp_offset = exp_offset_of(dtype, n);
+    memset(out, 0, bound); /* R10: every padding byte is zero */
+
+    uint8_t* exps = (uint8_t*)malloc(n ? n : 1);
+    if (!exps) return ORC_ERR_INVALID_ARG;
+    orc_split(dtype, in, n, exps, out + rem_offset);
+
+    uint64_t off = 0;
+    for (uint64_t c = 0; c < c_count; ++c) {
+        uint32_t n_c = chunk_elems(n, c);
+        uint32_t len = 0;
+        int raw = 0;
+        int st = orc_encode_chunk(exps + c * ORC_CHUNK_ELEMS, n_c, 0, out + exp_offset + off, &len, &raw);
+        if (st != ORC_OK) {
+            free(exps);
+            return st;
+        }
+        wr_le(out + ORC_HEADER_BYTES + 8u * c, off, 8);
+        wr_le(out + ORC_HEADER_BYTES + 8u * c_count + 4u * c, len | (raw ? ORC_RAW_FLAG : 0u), 4);
+        off += round16(len);
+    }
+    free(exps);
+
+    uint8_t* h = out;
+    h[0] = 'U';
+    h[1] = 'Z';
+    h[2] = 'P';
+    h[3] = '1';
+    wr_le(h + 4, 1, 2);
+    h[6] = (uint8_t)dtype;
+    h[7] = 0;
+    wr_le(h + 8, n, 8);
+    wr_le(h + 16, ORC_CHUNK_ELEMS, 4);
+    wr_le(h + 20, c_count, 4);
+    wr_le(h + 24, rem_offset, 8);
+    wr_le(h + 32, exp_offset, 8);
+    wr_le(h + 40, exp_offset + off, 8);
+    *total = exp_offset + off;
+    return ORC_OK;
+}
+
+/* R12: the receiver checks the header and every chunk before trusting it. */
+int orc_decompress(const uint8_t* comp, uint64_t comp_bytes, int dtype, uint64_t n, void* out) {
+    if (dtype != ORC_BF16 && dtype != ORC_FP32) return ORC_ERR_UNSUPPORTED_DTYPE;
+    if (comp == NULL || (n > 0 && out == NULL)) return ORC_ERR_INVALID_ARG;
+    if (comp_bytes < ORC_HEADER_BYTES) return ORC_ERR_CORRUPT;
+    const uint8_t* h = comp;
+    if (h[0] != 'U' || h[1] != 'Z' || h[2] != 'P' || h[3] != '1') return ORC_ERR_CORRUPT;
+    if (rd_le(h + 4, 2) != 1) return ORC_ERR_CORRUPT;
+    if (h[6] != (uint8_t)dtype || h[7] != 0) return ORC_ERR_CORRUPT;
+    if (rd_le(h + 8, 8) != n) return ORC_ERR_CORRUPT;
+    if (rd_le(h + 16, 4) != ORC_CHUNK_ELEMS) return ORC_ERR_CORRUPT;
+    uint64_t c_count = num_chunks(n);
+    if (rd_le(h + 20, 4) != c_count) return ORC_ERR_CORRUPT;
+    uint64_t rem_offset = rem_offset_of(n);
+    uint64_t exp_offset = exp_offset_of(dtype, n);
+    if (rd_le(h + 24, 8) != rem_offset) return ORC_ERR_CORRUPT;
+    if (rd_le(h + 32, 8) != exp_offset) return ORC_ERR_CORRUPT;
+    uint64_t total = rd_le(h + 40, 8);
+    if (total > comp_bytes || total < exp_offset) return ORC_ERR_CORRUPT;
+
+    uint8_t* exps = (uint8_t*)malloc(n ? n : 1);
+    if (!exps) return ORC_ERR_INVALID_ARG;
+    uint64_t section = total - exp_offset;
+    for (uint64_t c = 0; c < c_count; ++c) {
+        uint64_t off = rd_le(comp + ORC_HEADER_BYTES + 8u * c, 8);
+        uint32_t lw = (uint32_t)rd_le(comp + ORC_HEADER_BYTES + 8u * c_count + 4u * c, 4);
+        int raw = (lw & ORC_RAW_FLAG) != 0;
+        uint32_t len = lw & ~ORC_RAW_FLAG;
+        if (off % 16u != 0 || off > section || len > section - off) {
+            free(exps);
+            return ORC_ERR_CORRUPT;
+        }
+        int st = orc_decode_chunk(comp + exp_offset + off, len, raw, chunk_elems(n, c),
+                                  exps + c * ORC_CHUNK_ELEMS);
+        if (st != ORC_OK) {
+            free(exps);
+            return st;
+        }
+    }
+    int st = orc_merge(dtype, exps, comp + rem_offset, n, out);
+    free(exps);
+    return st;
+}
