@@ -1,0 +1,357 @@
+"""Benchmark: compress + decompress of a 1 GiB bf16 activation tensor on GB300.
+
+One step = the whole hot path over one tensor: plane split, histogram,
+normalisation, rANS encode, look-back placement (one fused compress kernel)
+and the table decoder with plane merge (one decompress kernel).  The
+workload is [8, 8192, 8192] bf16 ~ 0.5 * Student-t(4) with 1% outlier
+channels x50 and one random-bits chunk (the 1 GiB bf16 configuration).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  --impl reference times the oracle (single-threaded C)
+on a bounded sample of the same workload on the host cores.  Under torchrun
+every rank runs an independent replica (the codec has no exchange step);
+value = elements of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "compress & decompress GB/s (input bytes), ratio, % of HBM roofline, 1 GB300"
+WORKLOAD = ("c4: bf16 activations [8, 8192, 8192] ~ 0.5*Student-t(4), 82 outlier channels x50, "
+            "chunk 4096 random bits; 536,870,912 values (1 GiB)")
+KERNEL_SOURCES = ["lossless_float_tensor_gb300/csrc/compress.cu", "lossless_float_tensor_gb300/csrc/decompress.cu",
+                  "lossless_float_tensor_gb300/csrc/uzip_internal.cuh"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch_full")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [v for v in sm if mx and v >= 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(dev_index: int) -> str:
+    import torch
+
+    try:
+        u = torch.cuda.get_device_properties(dev_index).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev_index] if vis else str(dev_index)
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+    import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    bits = synth.c4()
+    n = bits.size
+    x = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    cap = uz.uzip_max_compressed_size(uz.UZIP_BF16, n)
+    comp = torch.empty(cap, dtype=torch.uint8, device=dev)
+    size = torch.zeros((), dtype=torch.int64, device=dev)
+    out = torch.empty_like(x)
+    status = torch.zeros((), dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    sp = stream.cuda_stream
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        st = uz.uzip_compress(x.data_ptr(), uz.UZIP_BF16, n, comp.data_ptr(), cap, size.data_ptr(), sp)
+        if ev is not None:
+            ev[1].record(stream)
+        st2 = uz.uzip_decompress(comp.data_ptr(), cap, out.data_ptr(), uz.UZIP_BF16, n, status.data_ptr(), sp)
+        if ev is not None:
+            ev[2].record(stream)
+        if st or st2:
+            raise RuntimeError(f"uzip status {st} {st2}")
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    total = int(size.item())
+    if int(status.item()) != 0 or not torch.equal(out.view(torch.int16), x.view(torch.int16)):
+        raise RuntimeError("round trip failed during warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_id_for(local_rank)) as clk:
+        t0 = time.perf_counter()
+        for k in range(args.steps):
+            step(events[k])
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    tc = [e[0].elapsed_time(e[1]) for e in events]
+    td = [e[1].elapsed_time(e[2]) for e in events]
+    step_ms = [e[0].elapsed_time(e[2]) for e in events]
+    dev_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([dev_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dev_ms = float(t.item())
+    ms_per_step = dev_ms / args.steps
+    in_bytes = 2 * n
+    value = world * in_bytes * args.steps / (dev_ms / 1e3) / 1e9
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, x, bits, comp, cap, size, out, status, stream, dev, total) if rank == 0 else None
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak_hbm()
+    mc, md = statistics.mean(tc), statistics.mean(td)
+    comp_bytes = in_bytes + total      # read input, write container
+    dec_bytes = total + in_bytes       # read container, write output
+    roof_c = {"bound": "hbm", "achieved": comp_bytes / (mc / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+              "frac": comp_bytes / (mc / 1e3) / 1e9 / peak, "traffic": profiled_traffic("compress"),
+              "kernel": "compress_kernel<bf16>", "algorithmic_bytes_per_launch": comp_bytes, "ms_per_launch": mc,
+              "peak_source": f"{peak_kind} hbm_gbs"}
+    roof_d = {"bound": "hbm", "achieved": dec_bytes / (md / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+              "frac": dec_bytes / (md / 1e3) / 1e9 / peak, "traffic": profiled_traffic("decompress"),
+              "kernel": "decompress_kernel<bf16>", "algorithmic_bytes_per_launch": dec_bytes, "ms_per_launch": md,
+              "peak_source": f"{peak_kind} hbm_gbs"}
+    dominant = roof_c if mc >= md else roof_d
+    cpu = None if args.no_cpu_baseline else cpu_baseline(bits)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "elements": n, "input_bytes": in_bytes, "parallelism": f"replicas x{world}",
+                   "l2": "inputs (1 GiB) larger than L2; no flush"},
+        "compress_gbs": in_bytes / (mc / 1e3) / 1e9, "decompress_gbs": in_bytes / (md / 1e3) / 1e9,
+        "ratio": total / in_bytes, "compressed_bytes": total,
+        "roofline": dominant, "roofline_compress": roof_c, "roofline_decompress": roof_d,
+        "clocks": clk.summary(), "e2e": e2e, "gpu_launches": 2 * args.steps,
+        "wall_s_timed_region": wall, "cpu_baseline": cpu, "kernel_source_hash": kernel_hash(),
+    }
+    return line
+
+
+def run_e2e(args, x, bits, comp, cap, size, out, status, stream, dev, total):
+    """H2D of the input from pinned memory, compress, D2H of the container,
+    H2D of the container, decompress, D2H of the output, every step."""
+    import numpy as np
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+
+    n = bits.size
+    h_in = torch.from_numpy(bits.view(np.int16)).pin_memory()
+    h_comp = torch.empty(cap, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(n, dtype=torch.int16).pin_memory()
+    h_size = torch.zeros((), dtype=torch.int64).pin_memory()
+    d_in = torch.empty(n, dtype=torch.int16, device=dev)
+    d_comp2 = torch.empty(cap, dtype=torch.uint8, device=dev)
+    sp = stream.cuda_stream
+    steps = max(1, min(args.steps, 5))
+
+    def one():
+        with torch.cuda.stream(stream):
+            d_in.copy_(h_in, non_blocking=True)
+            st = uz.uzip_compress(d_in.data_ptr(), uz.UZIP_BF16, n, comp.data_ptr(), cap, size.data_ptr(), sp)
+            h_size.copy_(size, non_blocking=True)
+        stream.synchronize()
+        tb = int(h_size.item())
+        with torch.cuda.stream(stream):
+            h_comp[:tb].copy_(comp[:tb], non_blocking=True)
+            d_comp2[:tb].copy_(h_comp[:tb], non_blocking=True)
+            st2 = uz.uzip_decompress(d_comp2.data_ptr(), tb, out.data_ptr(), uz.UZIP_BF16, n, status.data_ptr(), sp)
+            h_out.copy_(out.view(torch.int16), non_blocking=True)
+        stream.synchronize()
+        if st or st2:
+            raise RuntimeError("e2e status")
+        return tb
+
+    one()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    tb = 0
+    for _ in range(steps):
+        tb = one()
+    dt = (time.perf_counter() - t0) / steps
+    ok = bool(np.array_equal(h_out.numpy().view(np.uint16), bits))
+    return {"value": 2 * n / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": 2 * n + tb,
+            "d2h_bytes_per_step": tb + 2 * n + 8, "steps": steps, "bit_exact": ok}
+
+
+def cpu_baseline(bits):
+    """The oracle (single-threaded C) on the whole tensor, compress + decompress."""
+    import oracle
+
+    t0 = time.perf_counter()
+    c = oracle.compress(bits)
+    t1 = time.perf_counter()
+    oracle.decompress(c, oracle.BF16, bits.size)
+    t2 = time.perf_counter()
+    return {"value": 2 * bits.size / (t2 - t0) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"whole workload ({bits.size} values), compress {t1 - t0:.2f} s + decompress {t2 - t1:.2f} s",
+            "compress_gbs": 2 * bits.size / (t1 - t0) / 1e9, "decompress_gbs": 2 * bits.size / (t2 - t1) / 1e9}
+
+
+def run_reference(args):
+    """Reference arm: the oracle on the host cores, each step one bounded sample
+    (the first 256 chunks, 16,777,216 values) of the same workload."""
+    import oracle
+    import synth
+
+    bits = synth.c4(n=256 * 65536)
+    n = bits.size
+    times = []
+    for k in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        c = oracle.compress(bits)
+        oracle.decompress(c, oracle.BF16, n)
+        if k >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    per = sum(times) / len(times)
+    value = 2 * n / per / 1e9
+    cpu = {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": f"first 256 chunks ({n} values) of the workload per step"}
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "elements": n, "parallelism": "host, 1 thread"},
+            "ratio": c.size / (2 * n), "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import __graft_entry__
+
+    __graft_entry__.build_library()
+    if world > 1:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,160 @@
+/*
+ * uzip -- lossless compression of bf16 / fp32 GPU tensors (C ABI).
+ *
+ * What it computes.  Each value is split into its exponent field and the
+ * remaining sign and fraction bits; only the exponent field is entropy coded
+ * (with ANS), the remainder is stored raw (UCCL-Zip, arXiv 2604.17172,
+ * Fig. 2 caption).  Every chunk of work builds its own frequency table, so no
+ * global table or cross-block synchronisation is needed for the statistics
+ * (UCCL-Zip, Fig. 5 caption).  A chunk that coding does not shrink is stored
+ * RAW (NCCLZ, arXiv 2605.12396, Sec. IV-B/IV-C, Alg. 1), and the result is a
+ * self-describing frame, header plus payload (NCCLZ Sec. IV-B, IV-D2).
+ *
+ * Container (little endian):
+ *   [0,64)          header: "UZP1", u16 version = 1, u8 dtype, u8 flags = 0,
+ *                   u64 n, u32 chunk_elems = 65536, u32 num_chunks C,
+ *                   u64 rem_offset, u64 exp_offset, u64 total_bytes,
+ *                   16 zero bytes
+ *   [64, 64+8C)     u64 offset of chunk c's stream, relative to exp_offset
+ *   [64+8C, 64+12C) u32 length of chunk c's stream, bit 31 = stored RAW
+ *   rem_offset = round16(64 + 12C): remainder plane, n*rb bytes in element
+ *                   order (bf16: rb = 1, sign<<7 | fraction; fp32: rb = 3,
+ *                   sign<<23 | fraction, little endian)
+ *   exp_offset = round16(rem_offset + n*rb): one stream per chunk, each
+ *                   starting 16-byte aligned and zero padded to 16 bytes.
+ *   A coded stream is u32 state[32], u8 bitmap[32] of present exponent
+ *   bytes, u16 freq[K] (present bytes ascending, summing to 4096) and
+ *   u16 words[W]: 32 interleaved rANS states (32-bit, 16-bit renormalisation,
+ *   element i on lane i mod 32), the words listed in decoding order.  A RAW
+ *   stream is the chunk's exponent bytes.  Chunks hold 65536 elements (the
+ *   last may hold fewer).
+ *
+ * Conventions.
+ *   - Device pointers must be 16-byte aligned; the library never allocates:
+ *     the caller owns every buffer.
+ *   - Calls are stream ordered and asynchronous, except uzip_query_size,
+ *     which synchronises its stream.
+ *   - The return value reports argument and launch errors.  Data-dependent
+ *     errors (a corrupt container, a device-side wait that ran out) are
+ *     written to device memory (*d_status, *d_out_size = 0) and never trap.
+ *   - The input is never modified.
+ */
+#ifndef UZIP_H
+#define UZIP_H
+
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { UZIP_BF16 = 0, UZIP_FP32 = 1 } uzip_dtype;
+
+typedef enum {
+    UZIP_OK = 0,
+    UZIP_ERR_INVALID_ARG = 1,       /* null or misaligned pointer, n too large */
+    UZIP_ERR_UNSUPPORTED_DTYPE = 2, /* dtype not bf16 / fp32 */
+    UZIP_ERR_CAPACITY = 3,          /* output buffer smaller than required */
+    UZIP_ERR_CORRUPT = 4,           /* container failed validation */
+    UZIP_ERR_TIMEOUT = 5,           /* a bounded device-side wait ran out */
+    UZIP_ERR_CUDA = 6               /* a CUDA runtime call or launch failed */
+} uzip_status;
+
+/* Largest number of elements one call accepts (2^40). */
+#define UZIP_MAX_ELEMS (1ull << 40)
+
+/* Bytes the output buffer of uzip_compress must hold for (dtype, n): the
+ * largest possible container (every chunk stored RAW) plus the compressor's
+ * work area of 16 + 8*C bytes behind it.  Pure host function; returns 0 for
+ * an unsupported dtype or n > UZIP_MAX_ELEMS. */
+uint64_t uzip_max_compressed_size(uzip_dtype dtype, uint64_t n);
+
+/* Compress n elements at d_in into the container at d_out.
+ *   d_in          device, 16-byte aligned, n * (2 or 4) bytes; may be NULL
+ *                 when n == 0.
+ *   d_out         device, 16-byte aligned, out_capacity bytes; must be at
+ *                 least uzip_max_compressed_size(dtype, n) (else
+ *                 UZIP_ERR_CAPACITY).  On completion [0, total_bytes) is the
+ *                 container; the rest of the buffer is scratch.
+ *   d_out_size    device u64 (nullable): receives total_bytes, or 0 if a
+ *                 device-side wait ran out.
+ *   s             CUDA stream (0 = legacy default stream).
+ * Output bytes are a pure function of the input: the same input always gives
+ * the same container, equal byte for byte to the reference implementation. */
+uzip_status uzip_compress(const void* d_in, uzip_dtype dtype, uint64_t n, void* d_out,
+                          uint64_t out_capacity, uint64_t* d_out_size, cudaStream_t s);
+
+/* As uzip_compress, plus:
+ *   d_status  device i32 (nullable): 0 on success, else a uzip_status
+ *             (UZIP_ERR_TIMEOUT when a chunk's offset wait ran out).
+ *   flags     0 for normal use.  UZIP_TESTFLAG_SKIP_CHUNK0 makes the chunk
+ *             counter start at 1, so chunk 0 never publishes its length and
+ *             every wait on it runs out (about a second): it exists only to
+ *             test the timeout path; the container is then invalid. */
+#define UZIP_TESTFLAG_SKIP_CHUNK0 1u
+uzip_status uzip_compress_ex(const void* d_in, uzip_dtype dtype, uint64_t n, void* d_out,
+                             uint64_t out_capacity, uint64_t* d_out_size, int32_t* d_status,
+                             uint32_t flags, cudaStream_t s);
+
+/* Decompress the container at d_comp into n elements at d_out.
+ *   d_comp         device, 16-byte aligned; comp_capacity = readable bytes
+ *                  (at least the container's total_bytes).
+ *   d_out          device, 16-byte aligned, n * (2 or 4) bytes.
+ *   d_status       device i32 (nullable): set to 0, then to UZIP_ERR_CORRUPT
+ *                  if any check fails: header fields against (dtype, n),
+ *                  chunk offsets and lengths in range, frequency table sums
+ *                  to 4096 with every present entry >= 1, word reads stay in
+ *                  the stream, every lane ends in state 2^16 having used every
+ *                  word (NCCLZ Alg. 2 validates a frame before use).  On
+ *                  CORRUPT the contents of d_out are unspecified.
+ * Returns UZIP_ERR_CORRUPT at once (without a launch) if comp_capacity < 64. */
+uzip_status uzip_decompress(const void* d_comp, uint64_t comp_capacity, void* d_out,
+                            uzip_dtype dtype, uint64_t n, int32_t* d_status, cudaStream_t s);
+
+/* Read the 64-byte header of the container at d_comp (device) and return
+ * its total size, dtype and element count.  Synchronises s.  Returns
+ * UZIP_ERR_CORRUPT if the magic, version or layout fields do not check out,
+ * or total_bytes == 0 (a failed compression). Any output pointer may be NULL. */
+uzip_status uzip_query_size(const void* d_comp, uint64_t* h_total_bytes, uzip_dtype* h_dtype,
+                            uint64_t* h_n, cudaStream_t s);
+
+/* Static description of a status code. */
+const char* uzip_status_string(uzip_status st);
+
+/* ---------------------------------------------------------------------------
+ * Split-send pipeline on one GPU (UCCL-Zip Fig. 1 b and Fig. 4 d; NCCLZ
+ * Sec. IV-D4 ping-pong staging banks): message k is compressed on s_compress
+ * into device bank k % 2 while message k-1's container is copied to the host
+ * on s_copy.  The device-to-host copy stands in for the wire.
+ *
+ *   d_msgs[k], msg_elems[k]  device input of message k (16-byte aligned).
+ *   d_bank[2]                device banks, each bank_capacity bytes, at least
+ *                            uzip_max_compressed_size of the largest message.
+ *   h_bank[2]                pinned host banks (cudaHostAlloc / page-locked),
+ *                            h_capacity bytes each; message k's container
+ *                            lands in h_bank[k % 2] (a later message reuses
+ *                            the bank, as a sender's staging buffer would).
+ *   h_sizes                  pinned host u64[n_msgs]: container size of each
+ *                            message, written by the device (0 on failure).
+ *   mode                     UZIP_PIPE_EXACT: a copy kernel reads the size on
+ *                            the device and writes exactly total_bytes into
+ *                            the mapped host bank.  UZIP_PIPE_BOUND: one
+ *                            cudaMemcpyAsync of the size bound per message.
+ *                            UZIP_PIPE_SERIAL: compress then copy on one
+ *                            stream, no overlap (the naive design of UCCL-Zip
+ *                            Fig. 1 a), for comparison.
+ * Returns once all work is enqueued; the work ends when both streams drain.
+ * The caller must not reuse the banks until then. */
+typedef enum { UZIP_PIPE_EXACT = 0, UZIP_PIPE_BOUND = 1, UZIP_PIPE_SERIAL = 2 } uzip_pipe_mode;
+
+uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d_msgs, const uint64_t* msg_elems,
+                               uint32_t n_msgs, void* const* d_bank, uint64_t bank_capacity,
+                               void* const* h_bank, uint64_t h_capacity, uint64_t* h_sizes,
+                               uzip_pipe_mode mode, cudaStream_t s_compress, cudaStream_t s_copy);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* UZIP_H */

@@ -1,0 +1,30 @@
+/*
+ * uzip test hooks: host-only helpers that expose internal arithmetic of the
+ * library to its test-suite.  No GPU work; safe to call without a device.
+ * The pages have no counterpart: these exist to check the library's own
+ * implementation choices.
+ */
+#ifndef UZIP_DEBUG_H
+#define UZIP_DEBUG_H
+
+#include <stdint.h>
+
+#include "uzip.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The encoder replaces x / f (x in [16 f, f * 2^20), f in [1, 4096]) by
+ * (x * m + add) >> shift.  Returns 1 and the constants for a valid f, 0 for
+ * f outside [1, 4096]. */
+int uzip_debug_div_magic(uint32_t f, uint32_t* m, uint32_t* add, uint32_t* shift);
+
+/* Byte offset of the compressor's work area inside the output buffer (the
+ * area is 16 + 8*C bytes long and follows the largest possible container). */
+uint64_t uzip_debug_scratch_offset(uzip_dtype dtype, uint64_t n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,700 @@
+// Fused compressor: one warp per chunk of 65536 elements, one kernel for the
+// whole tensor (UCCL-Zip Fig. 5: local tables let the statistics, the coding
+// and the output placement run in one pass without cross-block
+// synchronisation).  Per chunk the warp
+//   1. streams the chunk once, writes its sign|fraction bytes straight to the
+//      remainder plane and counts exponent bytes in a lane-private histogram;
+//   2. normalises the histogram to 4096 (largest remainder) and builds the
+//      encode table;
+//   3. runs the 32-state interleaved rANS encoder backwards over the chunk,
+//      re-reading the exponents from L2, staging the words in shared memory;
+//   4. learns its output offset by a decoupled look-back over the chunks
+//      before it (Merrill and Garland, "Single-pass parallel prefix scan with
+//      decoupled look-back", 2016) and copies the staged stream out with
+//      16-byte stores.
+// A chunk whose stream does not fit the staging area is re-encoded twice
+// (count, then write in place); a chunk that coding does not shrink is stored
+// RAW (NCCLZ Sec. IV-C).
+#include "uzip_internal.cuh"
+
+namespace uzip {
+
+struct CompressArgs {
+    const uint8_t* in;
+    uint64_t n;
+    uint8_t* out;
+    Scratch* scratch;
+    uint64_t* desc;
+    uint64_t* out_size;   // nullable
+    int32_t* status_out;  // nullable
+    uint32_t first_ticket;
+    uint32_t num_chunks;
+};
+
+// element traits --------------------------------------------------------------
+template <int DT>
+struct Traits;
+template <>
+struct Traits<UZIP_BF16> {
+    static constexpr uint32_t kEs = 2;
+    __device__ static uint32_t exp_of(uint32_t b) { return (b >> 7) & 0xFFu; }
+    __device__ static uint32_t table_off(uint32_t b) { return (b >> 3) & 0xFF0u; }  // exponent * 16
+};
+template <>
+struct Traits<UZIP_FP32> {
+    static constexpr uint32_t kEs = 4;
+    __device__ static uint32_t exp_of(uint32_t b) { return (b >> 23) & 0xFFu; }
+    __device__ static uint32_t table_off(uint32_t b) { return (b >> 19) & 0xFF0u; }
+};
+
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t lane, uint32_t* total) {
+    uint32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= uint32_t(o)) inc += t;
+    }
+    *total = __shfl_sync(0xFFFFFFFFu, inc, 31);
+    return inc - v;
+}
+
+// ---------------------------------------------------------------------------
+// phase 1: plane split + lane-private histogram
+// hist layout: u32 [256 exponent values][32 lanes]; lane l only touches column
+// l, so the 32 increments of one instruction hit 32 distinct banks.
+template <int DT>
+__device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* __restrict__ rem_dst,
+                                uint8_t* hist, uint32_t lane, uint64_t pol_keep, uint64_t pol_stream) {
+    // zero the histogram: 32 KiB, 64 x 16 bytes per lane
+    {
+        uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll 8
+        for (uint32_t i = lane; i < kRegionA / 16; i += 32) reinterpret_cast<uint4*>(hist)[i] = z;
+    }
+    __syncwarp();
+    const uint32_t lane4 = lane * 4;
+    uint8_t* hl = hist + lane4;
+    constexpr uint32_t kPer = 16 / Traits<DT>::kEs;  // elements per 16-byte load
+    const uint32_t nvec = n_c / kPer;
+    constexpr int U = 8;
+    uint32_t v = lane;
+    for (; v + 32 * (U - 1) < nvec; v += 32 * U) {
+        uint4 q[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) q[u] = ld_v4_hint(cin + uint64_t(v + 32 * u) * 16, pol_keep);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+            const uint32_t vi = v + 32 * u;
+            if (DT == UZIP_BF16) {
+                uint32_t r[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    r[j] = ((w[j] >> 8) & 0x00800080u) | (w[j] & 0x007F007Fu);
+                    atomicAdd(reinterpret_cast<uint32_t*>(hl + (w[j] & 0x7F80u)), 1u);
+                    atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
+                }
+                st_v2_hint(rem_dst + uint64_t(vi) * 8, __byte_perm(r[0], r[1], 0x6420), __byte_perm(r[2], r[3], 0x6420),
+                           pol_stream);
+            } else {
+                uint32_t r[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    r[j] = (w[j] & 0x7FFFFFu) | ((w[j] >> 8) & 0x800000u);
+                    atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
+                }
+                uint8_t* d = rem_dst + uint64_t(vi) * 12;
+                st_u32_hint(d, r[0] | (r[1] << 24), pol_stream);
+                st_u32_hint(d + 4, (r[1] >> 8) | (r[2] << 16), pol_stream);
+                st_u32_hint(d + 8, (r[2] >> 16) | (r[3] << 8), pol_stream);
+            }
+        }
+    }
+    for (; v < nvec; v += 32) {
+        uint4 q = ld_v4_hint(cin + uint64_t(v) * 16, pol_keep);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        if (DT == UZIP_BF16) {
+            uint32_t r[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                r[j] = ((w[j] >> 8) & 0x00800080u) | (w[j] & 0x007F007Fu);
+                atomicAdd(reinterpret_cast<uint32_t*>(hl + (w[j] & 0x7F80u)), 1u);
+                atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
+            }
+            st_v2_hint(rem_dst + uint64_t(v) * 8, __byte_perm(r[0], r[1], 0x6420), __byte_perm(r[2], r[3], 0x6420),
+                       pol_stream);
+        } else {
+            uint32_t r[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                r[j] = (w[j] & 0x7FFFFFu) | ((w[j] >> 8) & 0x800000u);
+                atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
+            }
+            uint8_t* d = rem_dst + uint64_t(v) * 12;
+            st_u32_hint(d, r[0] | (r[1] << 24), pol_stream);
+            st_u32_hint(d + 4, (r[1] >> 8) | (r[2] << 16), pol_stream);
+            st_u32_hint(d + 8, (r[2] >> 16) | (r[3] << 8), pol_stream);
+        }
+    }
+    // ragged tail: element by element
+    for (uint32_t i = nvec * kPer + lane; i < n_c; i += 32) {
+        if (DT == UZIP_BF16) {
+            const uint32_t b = reinterpret_cast<const uint16_t*>(cin)[i];
+            rem_dst[i] = uint8_t(((b >> 8) & 0x80u) | (b & 0x7Fu));
+            atomicAdd(reinterpret_cast<uint32_t*>(hl + (b & 0x7F80u)), 1u);
+        } else {
+            const uint32_t b = reinterpret_cast<const uint32_t*>(cin)[i];
+            const uint32_t r = (b & 0x7FFFFFu) | ((b >> 8) & 0x800000u);
+            rem_dst[3 * uint64_t(i)] = uint8_t(r);
+            rem_dst[3 * uint64_t(i) + 1] = uint8_t(r >> 8);
+            rem_dst[3 * uint64_t(i) + 2] = uint8_t(r >> 16);
+            atomicAdd(reinterpret_cast<uint32_t*>(hl + ((b >> 16) & 0x7F80u)), 1u);
+        }
+    }
+    __syncwarp();
+}
+
+// counts of symbols 8*lane .. 8*lane+7 from the lane-private histogram; the
+// column order is staggered by lane so each quarter-warp reads 8 distinct
+// 16-byte groups (no bank conflicts).
+__device__ void reduce_hist(const uint8_t* hist, uint32_t lane, uint32_t c[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint8_t* row = hist + (8 * lane + k) * 128;
+        uint32_t s = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint4 q = *reinterpret_cast<const uint4*>(row + ((j + lane) & 7) * 16);
+            s += q.x + q.y + q.z + q.w;
+        }
+        c[k] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// phase 2: largest-remainder normalisation (rule R5) -- lane owns symbols
+// 8*lane + k.  Leaves f in registers and in freq[] (shared), returns K.
+struct Norm {
+    uint32_t f[8];
+    uint32_t present;  // 8-bit mask of present symbols of this lane
+    uint32_t prefix;   // present symbols of lower lanes
+    uint32_t k_total;  // present symbols overall
+};
+
+__device__ void normalise(const uint32_t c[8], uint32_t n_c, uint32_t lane, uint8_t* regB, Norm& nm) {
+    uint16_t* freq = reinterpret_cast<uint16_t*>(regB);          // u16[256]
+    uint32_t* keys = reinterpret_cast<uint32_t*>(regB + 512);    // u32[256]
+    uint32_t r[8];
+    uint32_t boosted = 0, present = 0, fsum = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        uint32_t f, rr;
+        if (n_c == kChunk) {
+            f = c[k] >> 4;
+            rr = (c[k] & 15u) << 12;
+        } else {
+            const uint32_t scaled = c[k] * kM;
+            f = scaled / n_c;
+            rr = scaled - f * n_c;
+        }
+        if (c[k]) {
+            present |= 1u << k;
+            if (f == 0) {
+                f = 1;
+                boosted |= 1u << k;
+            }
+        }
+        nm.f[k] = f;
+        r[k] = rr;
+        fsum += f;
+    }
+    const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, fsum);
+    if (total < kM) {
+        // candidates: present, not boosted; key orders by (remainder desc, symbol asc)
+        const uint32_t cand = present & ~boosted;
+        uint32_t nc_total;
+        const uint32_t base = warp_excl_scan(__popc(cand), lane, &nc_total);
+        uint32_t idx = base;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (cand & (1u << k)) keys[idx++] = (r[k] << 8) | (255u - (8 * lane + k));
+        __syncwarp();
+        const uint32_t need = kM - total;
+        // candidate i is ranked by lane i % 32
+        for (uint32_t i = lane; i < nc_total; i += 32) {
+            const uint32_t key = keys[i];
+            uint32_t rank = 0;
+            for (uint32_t j = 0; j < nc_total; ++j) rank += keys[j] > key ? 1u : 0u;
+            // freq[] doubles as a winner flag for candidates until it is rewritten below
+            freq[255u - (key & 0xFFu)] = rank < need ? 1 : 0;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (cand & (1u << k)) nm.f[k] += freq[8 * lane + k];
+        __syncwarp();
+    } else if (total > kM) {
+        uint32_t excess = total - kM;
+        while (excess--) {
+            uint32_t best = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t key = (nm.f[k] << 8) | (255u - (8 * lane + k));
+                best = key > best ? key : best;
+            }
+            const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
+            const uint32_t s = 255u - (top & 0xFFu);
+            if ((s >> 3) == lane) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (uint32_t(k) == (s & 7u)) nm.f[k] -= 1;
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) freq[8 * lane + k] = uint16_t(nm.f[k]);
+    nm.present = present;
+    uint32_t ktot;
+    nm.prefix = warp_excl_scan(__popc(present), lane, &ktot);
+    nm.k_total = ktot;
+    regB[1536 + lane] = uint8_t(present);  // bitmap byte `lane` = symbols 8*lane..8*lane+7
+    __syncwarp();
+}
+
+// encode table entry for each present symbol: {m, add, (f << 20) - 1, (M - f) | cum << 12 | sh << 27}
+__device__ void build_enc_table(const Norm& nm, uint32_t lane, uint8_t* table, uint8_t* regB) {
+    uint32_t lsum = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) lsum += nm.f[k];
+    uint32_t dummy;
+    uint32_t cum = warp_excl_scan(lsum, lane, &dummy);
+    // present symbol list (u8) in shared memory, then one symbol per lane
+    uint8_t* plist = regB + 1600;  // 256 bytes
+    uint32_t* cums = reinterpret_cast<uint32_t*>(regB + 512);  // reuse the key area: u32 cum per symbol
+    uint32_t idx = nm.prefix;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (nm.present & (1u << k)) {
+            plist[idx++] = uint8_t(8 * lane + k);
+            cums[8 * lane + k] = cum;
+        }
+        cum += nm.f[k];
+    }
+    __syncwarp();
+    const uint16_t* freq = reinterpret_cast<const uint16_t*>(regB);
+    for (uint32_t i = lane; i < nm.k_total; i += 32) {
+        const uint32_t s = plist[i];
+        const uint32_t f = freq[s];
+        const DivMagic dm = div_magic(f);
+        uint4 e;
+        e.x = dm.m;
+        e.y = dm.add;
+        e.z = uint32_t((uint64_t(f) << 20) - 1);
+        e.w = (kM - f) | (cums[s] << 12) | (dm.sh << 27);
+        *reinterpret_cast<uint4*>(table + 16 * s) = e;
+    }
+    __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// one rANS encode step for one lane (rule R6); returns the renormalisation
+// predicate.  entry = encode table row of the lane's symbol.
+__device__ __forceinline__ uint32_t rans_update(uint32_t x, const uint4 e, bool emit) {
+    const uint32_t xr = emit ? (x >> 16) : x;
+    const uint32_t sh = e.w >> 27;
+    const uint64_t t = uint64_t(xr) * e.x + e.y;
+    const uint32_t q = uint32_t(t >> 32) >> sh;
+    const uint32_t mmf = e.w & 0xFFFu;
+    const uint32_t cum = (e.w >> 12) & 0xFFFu;
+    return xr + q * mmf + cum;
+}
+
+enum class Sink { Smem, Count, Global };
+
+// Encodes steps t = T-1 .. 0.  Sink::Smem stages words below *pos (u16 index
+// into region A) and returns false if the staging would pass `limit`;
+// Sink::Count only counts words and returns false once the coded length
+// reaches n_c (the chunk goes RAW); Sink::Global writes words to gwords in
+// place, *pos counting down from W.
+template <int DT, Sink S>
+__device__ bool encode_chunk(const uint8_t* __restrict__ cin, uint32_t n_c, const uint8_t* table, uint16_t* stage,
+                             uint32_t lane, uint32_t& x_out, int32_t& pos, int32_t limit, uint8_t* gwords,
+                             uint32_t hdr_bytes, uint64_t pol) {
+    constexpr uint32_t es = Traits<DT>::kEs;
+    const uint32_t T = (n_c + 31) / 32;
+    const uint32_t lt = lanemask_lt();
+    uint32_t x = kRansL;
+    auto load = [&](uint32_t t) -> uint32_t {
+        const uint32_t i = 32 * t + lane;
+        if (i >= n_c) return 0;
+        return es == 2 ? ld_u16_hint(cin + 2 * uint64_t(i), pol) : ld_u32_hint(cin + 4 * uint64_t(i), pol);
+    };
+    auto step = [&](uint32_t bits, bool active) -> bool {
+        const uint4 e = *reinterpret_cast<const uint4*>(table + Traits<DT>::table_off(bits));
+        const bool emit = active && (x > e.z);
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, emit);
+        const int32_t nt = __popc(b);
+        if (S == Sink::Smem) {
+            if (pos - nt < limit) return false;
+            if (emit) stage[pos - nt + __popc(b & lt)] = uint16_t(x);
+        } else if (S == Sink::Global) {
+            if (emit) {
+                const uint32_t wi = uint32_t(pos - nt) + __popc(b & lt);
+                *reinterpret_cast<uint16_t*>(gwords + 2 * uint64_t(wi)) = uint16_t(x);
+            }
+        }
+        pos -= nt;
+        if (S == Sink::Count) {
+            // pos counts down from 0: -pos words so far
+            if (hdr_bytes + 2 * uint32_t(-pos) >= n_c) return false;
+        }
+        const uint32_t xn = rans_update(x, e, emit);
+        x = active ? xn : x;
+        return true;
+    };
+    if (n_c == kChunk) {
+        // full chunk: 2048 steps, prefetch 32 steps ahead in two register banks
+        uint32_t a[32], bnk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) a[j] = load(kSteps - 1 - j);
+        for (int32_t t0 = kSteps - 1; t0 >= 0; t0 -= 64) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) bnk[j] = (t0 - 32 - j >= 0) ? load(t0 - 32 - j) : 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (!step(a[j], true)) {
+                    x_out = x;
+                    return false;
+                }
+            if (t0 - 32 < 0) break;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] = (t0 - 64 - j >= 0) ? load(t0 - 64 - j) : 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (!step(bnk[j], true)) {
+                    x_out = x;
+                    return false;
+                }
+        }
+    } else {
+        for (int32_t t = int32_t(T) - 1; t >= 0; --t) {
+            const uint32_t bits = load(uint32_t(t));
+            if (!step(bits, 32 * uint32_t(t) + lane < n_c)) {
+                x_out = x;
+                return false;
+            }
+        }
+    }
+    x_out = x;
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// output helpers
+
+// header of a coded stream: 32 states, bitmap, present frequencies ascending
+__device__ void write_stream_head_smem(uint8_t* dst, uint32_t x, const Norm& nm, uint32_t lane, const uint8_t* regB) {
+    uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);  // dst is 2-byte aligned
+    d16[2 * lane] = uint16_t(x);
+    d16[2 * lane + 1] = uint16_t(x >> 16);
+    if (lane < 16) d16[64 + lane] = uint16_t(regB[1536 + 2 * lane] | (regB[1536 + 2 * lane + 1] << 8));
+    uint32_t idx = nm.prefix;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (nm.present & (1u << k)) d16[80 + idx++] = uint16_t(nm.f[k]);
+}
+
+// copy `len` bytes from shared (2-byte aligned, ending at `end`) to global
+// (16-byte aligned), zero padding the last 16-byte block.
+__device__ void copy_record_out(const uint8_t* src, uint32_t len, const uint8_t* end, uint8_t* dst, uint32_t lane) {
+    const uint32_t nb = (len + 15) / 16;
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src);
+    const uint32_t mis = uint32_t(s0 & 3u);  // 0 or 2
+    for (uint32_t b = lane; b < nb; b += 32) {
+        const uint8_t* sb = src + 16 * b;
+        const uint32_t* wp = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(sb) & ~uintptr_t(3));
+        uint32_t w[5];
+#pragma unroll
+        for (int j = 0; j < 5; ++j) {
+            const uint8_t* a = reinterpret_cast<const uint8_t*>(wp + j);
+            w[j] = a < end ? wp[j] : 0u;
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = mis ? __byte_perm(w[j], w[j + 1], 0x5432) : w[j];
+        const uint32_t valid = len - 16 * b;  // bytes of this block inside the record
+        if (valid < 16) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t lo = 4 * j;
+                if (valid <= lo) o[j] = 0;
+                else if (valid < lo + 4) o[j] &= (1u << (8 * (valid - lo))) - 1u;
+            }
+        }
+        *reinterpret_cast<uint4*>(dst + 16 * b) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// RAW chunk: the n_c exponent bytes, zero padded to 16
+template <int DT>
+__device__ void write_raw(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* dst, uint32_t lane) {
+    const uint32_t nb = (n_c + 15) / 16;
+    for (uint32_t b = lane; b < nb; b += 32) {
+        const uint32_t i0 = 16 * b;
+        uint32_t o[4] = {0, 0, 0, 0};
+        if (i0 + 16 <= n_c) {
+            if (DT == UZIP_BF16) {
+                const uint4 q0 = *reinterpret_cast<const uint4*>(cin + 2 * uint64_t(i0));
+                const uint4 q1 = *reinterpret_cast<const uint4*>(cin + 2 * uint64_t(i0) + 16);
+                const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    o[j] = __byte_perm((w[2 * j] >> 7) & 0x00FF00FFu, (w[2 * j + 1] >> 7) & 0x00FF00FFu, 0x6420);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 q = *reinterpret_cast<const uint4*>(cin + 4 * uint64_t(i0) + 16 * j);
+                    o[j] = (q.x >> 23 & 0xFFu) | ((q.y >> 23 & 0xFFu) << 8) | ((q.z >> 23 & 0xFFu) << 16) |
+                           ((q.w >> 23 & 0xFFu) << 24);
+                }
+            }
+        } else {
+            for (uint32_t k = 0; k < 16 && i0 + k < n_c; ++k) {
+                const uint32_t bits = DT == UZIP_BF16 ? reinterpret_cast<const uint16_t*>(cin)[i0 + k]
+                                                      : reinterpret_cast<const uint32_t*>(cin)[i0 + k];
+                o[k >> 2] |= Traits<DT>::exp_of(bits) << (8 * (k & 3));
+            }
+        }
+        *reinterpret_cast<uint4*>(dst + 16 * uint64_t(b)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// decoupled look-back: exclusive prefix of padded stream lengths before chunk c
+__device__ bool look_back(uint64_t* desc, uint32_t c, uint64_t padded, uint32_t lane, uint64_t& excl_out) {
+    if (c == 0) {
+        if (lane == 0) st_release_u64(desc, kDescInclusive | padded);
+        excl_out = 0;
+        return true;
+    }
+    if (lane == 0) st_release_u64(desc + c, kDescAggregate | padded);
+    uint64_t excl = 0;
+    int64_t top = int64_t(c) - 1;
+    uint32_t spins = 0;
+    uint32_t backoff = 32;
+    bool ok = true;
+    while (true) {
+        const int64_t idx = top - int64_t(lane);
+        const uint64_t d = idx >= 0 ? ld_acquire_u64(desc + idx) : kDescInclusive;
+        const uint32_t flag = uint32_t(d >> 62);
+        const uint32_t incl = __ballot_sync(0xFFFFFFFFu, flag == 2);
+        const uint32_t empty = __ballot_sync(0xFFFFFFFFu, flag == 0);
+        const uint32_t first = incl ? uint32_t(__ffs(incl) - 1) : 32u;
+        const uint32_t below = first == 32 ? 0xFFFFFFFFu : ((1u << first) - 1u);
+        if (empty & below) {
+            if (++spins > kSpinLimit) {
+                ok = false;
+                break;
+            }
+            __nanosleep(backoff);
+            backoff = backoff < 1024 ? backoff * 2 : 1024;
+            continue;
+        }
+        const uint64_t val = lane <= first ? (d & kDescValue) : 0;
+        excl += warp_sum_u64(val);
+        if (first < 32) break;
+        top -= 32;
+    }
+    if (lane == 0) st_release_u64(desc + c, kDescInclusive | ((excl + padded) & kDescValue));
+    excl_out = excl;
+    return ok;
+}
+
+// ---------------------------------------------------------------------------
+template <int DT>
+__global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint8_t* regA = smem;
+    uint8_t* regB = smem + kRegionA;
+    const uint32_t lane = threadIdx.x;
+    const uint64_t n = a.n;
+    const uint32_t C = a.num_chunks;
+    const uint64_t rem_off = rem_offset(n);
+    const uint64_t exp_off = exp_offset(DT, n);
+    constexpr uint32_t es = Traits<DT>::kEs;
+    constexpr uint32_t rb = DT == UZIP_BF16 ? 1 : 3;
+    const uint64_t pol_keep = policy_evict_last();
+    const uint64_t pol_stream = policy_evict_first();
+    const uint32_t processed = C - a.first_ticket;
+
+    uint32_t* ticket = &a.scratch->ticket;
+    while (C > 0) {
+        uint32_t c = 0;
+        if (lane == 0) c = atomicAdd(ticket, 1u) + a.first_ticket;
+        c = __shfl_sync(0xFFFFFFFFu, c, 0);
+        if (c >= C) break;
+        const uint64_t left = n - uint64_t(c) * kChunk;
+        const uint32_t n_c = uint32_t(left < kChunk ? left : kChunk);
+        const uint8_t* cin = a.in + uint64_t(c) * kChunk * es;
+
+        // 1. plane split + histogram
+        split_and_count<DT>(cin, n_c, a.out + rem_off + uint64_t(c) * kChunk * rb, regA, lane, pol_keep, pol_stream);
+        uint32_t cnt[8];
+        reduce_hist(regA, lane, cnt);
+        __syncwarp();
+        // 2. normalise + encode table
+        Norm nm;
+        normalise(cnt, n_c, lane, regB, nm);
+        build_enc_table(nm, lane, regA, regB);
+        const uint32_t hdr = kStreamHead + 2 * nm.k_total;
+
+        // 3. encode into shared staging
+        uint32_t x = kRansL;
+        int32_t pos = int32_t(kRegionA / 2);
+        const int32_t limit = int32_t((kStageBase + hdr) / 2);
+        uint16_t* stage = reinterpret_cast<uint16_t*>(regA);
+        const bool fits = encode_chunk<DT, Sink::Smem>(cin, n_c, regA, stage, lane, x, pos, limit, nullptr, hdr, pol_stream);
+
+        uint32_t len = 0;
+        bool raw = false;
+        uint32_t w_total = 0;
+        if (fits) {
+            w_total = kRegionA / 2 - uint32_t(pos);
+            len = hdr + 2 * w_total;
+            raw = len >= n_c;
+        } else {
+            int32_t cpos = 0;
+            uint32_t xc;
+            const bool coded = encode_chunk<DT, Sink::Count>(cin, n_c, regA, nullptr, lane, xc, cpos, 0, nullptr, hdr, pol_stream);
+            w_total = uint32_t(-cpos);
+            len = hdr + 2 * w_total;
+            raw = !coded || len >= n_c;
+        }
+        if (raw) len = n_c;
+
+        // 4. offset by decoupled look-back
+        uint64_t excl = 0;
+        const bool ok = look_back(a.desc, c, round16(len), lane, excl);
+        if (!ok && lane == 0) atomicCAS(&a.scratch->status, 0u, uint32_t(UZIP_ERR_TIMEOUT));
+        if (ok) {
+            uint8_t* dst = a.out + exp_off + excl;
+            if (raw) {
+                write_raw<DT>(cin, n_c, dst, lane);
+            } else if (fits) {
+                uint8_t* rec = regA + 2 * uint32_t(pos) - hdr;
+                write_stream_head_smem(rec, x, nm, lane, regB);
+                __syncwarp();
+                copy_record_out(rec, len, regA + kRegionA, dst, lane);
+            } else {
+                // re-encode, writing the words in place behind the stream head
+                int32_t gpos = int32_t(w_total);
+                uint32_t xg;
+                encode_chunk<DT, Sink::Global>(cin, n_c, regA, nullptr, lane, xg, gpos, 0, dst + hdr, hdr, pol_stream);
+                uint8_t* rec = regA + kStageBase;  // staging is free now: build the head there
+                write_stream_head_smem(rec, xg, nm, lane, regB);
+                __syncwarp();
+                for (uint32_t i = lane; i < hdr / 2; i += 32)
+                    reinterpret_cast<uint16_t*>(dst)[i] = reinterpret_cast<const uint16_t*>(rec)[i];
+                for (uint32_t i = len + lane; i < round16(len); i += 32) dst[i] = 0;
+            }
+            if (lane == 0) {
+                reinterpret_cast<uint64_t*>(a.out + kHeader)[c] = excl;
+                reinterpret_cast<uint32_t*>(a.out + kHeader + 8 * uint64_t(C))[c] = len | (raw ? kRawFlag : 0u);
+            }
+        }
+        __syncwarp();
+        // 5. the last chunk to finish writes the header
+        uint32_t prev = 0;
+        if (lane == 0) {
+            __threadfence();
+            prev = atomicAdd(&a.scratch->done, 1u);
+        }
+        prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+        if (prev + 1 != processed) continue;
+        __threadfence();
+        if (lane == 0) {
+            const uint32_t st = *reinterpret_cast<volatile uint32_t*>(&a.scratch->status);
+            const uint64_t last = ld_acquire_u64(a.desc + (C - 1));
+            uint64_t total = exp_off + (last & kDescValue);
+            if (st != 0 || (last >> 62) != 2) total = 0;
+            uint8_t* h = a.out;
+            *reinterpret_cast<uint32_t*>(h) = 0x31505A55u;  // "UZP1"
+            *reinterpret_cast<uint16_t*>(h + 4) = 1;
+            h[6] = uint8_t(DT);
+            h[7] = 0;
+            *reinterpret_cast<uint64_t*>(h + 8) = n;
+            *reinterpret_cast<uint32_t*>(h + 16) = kChunk;
+            *reinterpret_cast<uint32_t*>(h + 20) = C;
+            *reinterpret_cast<uint64_t*>(h + 24) = rem_off;
+            *reinterpret_cast<uint64_t*>(h + 32) = exp_off;
+            *reinterpret_cast<uint64_t*>(h + 40) = total;
+            *reinterpret_cast<uint64_t*>(h + 48) = 0;
+            *reinterpret_cast<uint64_t*>(h + 56) = 0;
+            for (uint64_t i = kHeader + 12 * uint64_t(C); i < rem_off; ++i) h[i] = 0;
+            for (uint64_t i = rem_off + n * rb; i < exp_off; ++i) h[i] = 0;
+            if (a.out_size) *a.out_size = total;
+            if (a.status_out) *a.status_out = int32_t(st ? st : (total ? 0u : uint32_t(UZIP_ERR_TIMEOUT)));
+        }
+        break;
+    }
+    // empty tensor: header only, written by the single launched warp
+    if (C == 0 && blockIdx.x == 0 && lane == 0) {
+        uint8_t* h = a.out;
+        *reinterpret_cast<uint32_t*>(h) = 0x31505A55u;
+        *reinterpret_cast<uint16_t*>(h + 4) = 1;
+        h[6] = uint8_t(DT);
+        h[7] = 0;
+        *reinterpret_cast<uint64_t*>(h + 8) = 0;
+        *reinterpret_cast<uint32_t*>(h + 16) = kChunk;
+        *reinterpret_cast<uint32_t*>(h + 20) = 0;
+        *reinterpret_cast<uint64_t*>(h + 24) = kHeader;
+        *reinterpret_cast<uint64_t*>(h + 32) = kHeader;
+        *reinterpret_cast<uint64_t*>(h + 40) = kHeader;
+        *reinterpret_cast<uint64_t*>(h + 48) = 0;
+        *reinterpret_cast<uint64_t*>(h + 56) = 0;
+        if (a.out_size) *a.out_size = kHeader;
+        if (a.status_out) *a.status_out = 0;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host launcher (called by the C ABI after argument checks)
+cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
+                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s) {
+    const uint64_t C = num_chunks(n);
+    uint8_t* out = static_cast<uint8_t*>(d_out);
+    Scratch* scratch = reinterpret_cast<Scratch*>(out + scratch_offset(dtype, n));
+    cudaError_t err = cudaMemsetAsync(scratch, 0, scratch_bytes(n), s);
+    if (err != cudaSuccess) return err;
+    CompressArgs a;
+    a.in = static_cast<const uint8_t*>(d_in);
+    a.n = n;
+    a.out = out;
+    a.scratch = scratch;
+    a.desc = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(scratch) + kScratchHead);
+    a.out_size = d_out_size;
+    a.status_out = d_status;
+    a.first_ticket = C > 0 ? (first_ticket < C ? first_ticket : uint32_t(C - 1)) : 0;
+    a.num_chunks = uint32_t(C);
+
+    int dev = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    int sms = 0;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    void (*kern)(CompressArgs) = dtype == UZIP_BF16 ? compress_kernel<UZIP_BF16> : compress_kernel<UZIP_FP32>;
+    int per_sm = 0;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, kCompressSmem)) != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+    uint64_t grid = uint64_t(per_sm) * uint64_t(sms);
+    const uint64_t work = C > a.first_ticket ? C - a.first_ticket : 1;
+    if (grid > work) grid = work;
+    if (grid < 1) grid = 1;
+    kern<<<dim3(uint32_t(grid)), dim3(32), kCompressSmem, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace uzip

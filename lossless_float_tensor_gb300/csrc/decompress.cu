@@ -1,0 +1,306 @@
+// Decompressor: one warp per chunk, chunks strided over a persistent grid.
+// Per chunk the warp validates the chunk-table entry and the stream head,
+// builds the 4096-slot symbol table in shared memory, runs the 32 interleaved
+// rANS decoders forward, and merges each decoded exponent byte with its
+// sign|fraction bits from the remainder plane into the output value (the
+// receive side of UCCL-Zip's split-send and of NCCLZ Alg. 2, which validates a
+// frame before using it).
+#include "uzip_internal.cuh"
+
+namespace uzip {
+
+struct DecompressArgs {
+    const uint8_t* comp;
+    uint64_t cap;
+    uint8_t* out;
+    uint64_t n;
+    int32_t* status;  // nullable
+};
+
+__device__ __forceinline__ void flag_corrupt(int32_t* status) {
+    if (status) atomicCAS(reinterpret_cast<int*>(status), 0, int(UZIP_ERR_CORRUPT));
+}
+
+__device__ __forceinline__ uint32_t warp_excl_scan_d(uint32_t v, uint32_t lane, uint32_t* total) {
+    uint32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= uint32_t(o)) inc += t;
+    }
+    *total = __shfl_sync(0xFFFFFFFFu, inc, 31);
+    return inc - v;
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t merge_bits(uint32_t e, uint32_t r) {
+    if (DT == UZIP_BF16) return ((r & 0x80u) << 8) | (e << 7) | (r & 0x7Fu);
+    return ((r & 0x800000u) << 8) | (e << 23) | (r & 0x7FFFFFu);
+}
+
+template <int DT>
+__device__ void merge_raw(const uint8_t* __restrict__ ex, const uint8_t* __restrict__ rem, uint8_t* __restrict__ out,
+                          uint32_t n_c, uint32_t lane) {
+    constexpr uint32_t rb = DT == UZIP_BF16 ? 1 : 3;
+    constexpr uint32_t es = DT == UZIP_BF16 ? 2 : 4;
+    const uint32_t nfull = n_c / 16;
+    for (uint32_t b = lane; b < nfull; b += 32) {
+        const uint4 eq = *reinterpret_cast<const uint4*>(ex + 16 * uint64_t(b));
+        const uint32_t ew[4] = {eq.x, eq.y, eq.z, eq.w};
+        uint32_t rw[12];
+        if (DT == UZIP_BF16) {
+            const uint4 rq = *reinterpret_cast<const uint4*>(rem + 16 * uint64_t(b));
+            rw[0] = rq.x, rw[1] = rq.y, rw[2] = rq.z, rw[3] = rq.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                const uint4 rq = *reinterpret_cast<const uint4*>(rem + 48 * uint64_t(b) + 16 * j);
+                rw[4 * j] = rq.x, rw[4 * j + 1] = rq.y, rw[4 * j + 2] = rq.z, rw[4 * j + 3] = rq.w;
+            }
+        }
+        uint32_t o[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const uint32_t e = (ew[k >> 2] >> (8 * (k & 3))) & 0xFFu;
+            uint32_t r;
+            if (DT == UZIP_BF16) {
+                r = (rw[k >> 2] >> (8 * (k & 3))) & 0xFFu;
+            } else {
+                const uint32_t byte0 = 3 * k;
+                r = 0;
+#pragma unroll
+                for (int q = 0; q < 3; ++q) r |= ((rw[(byte0 + q) >> 2] >> (8 * ((byte0 + q) & 3))) & 0xFFu) << (8 * q);
+            }
+            o[k] = merge_bits<DT>(e, r);
+        }
+        if (DT == UZIP_BF16) {
+            uint4* d = reinterpret_cast<uint4*>(out + 32 * uint64_t(b));
+            d[0] = make_uint4(o[0] | o[1] << 16, o[2] | o[3] << 16, o[4] | o[5] << 16, o[6] | o[7] << 16);
+            d[1] = make_uint4(o[8] | o[9] << 16, o[10] | o[11] << 16, o[12] | o[13] << 16, o[14] | o[15] << 16);
+        } else {
+            uint4* d = reinterpret_cast<uint4*>(out + 64 * uint64_t(b));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) d[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        }
+    }
+    for (uint32_t i = nfull * 16 + lane; i < n_c; i += 32) {
+        uint32_t r = rem[rb * uint64_t(i)];
+        if (DT == UZIP_FP32) r |= uint32_t(rem[3 * uint64_t(i) + 1]) << 8 | uint32_t(rem[3 * uint64_t(i) + 2]) << 16;
+        const uint32_t v = merge_bits<DT>(ex[i], r);
+        if (es == 2) reinterpret_cast<uint16_t*>(out)[i] = uint16_t(v);
+        else reinterpret_cast<uint32_t*>(out)[i] = v;
+    }
+}
+
+// Coded chunk.  Returns false if the stream is invalid.
+template <int DT>
+__device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, const uint8_t* __restrict__ rem,
+                             uint8_t* __restrict__ out, uint32_t n_c, uint32_t lane, uint8_t* wsm) {
+    constexpr uint32_t es = DT == UZIP_BF16 ? 2 : 4;
+    uint8_t* slot_sym = wsm;                                                   // u8[4096]
+    uint32_t* sym_fc = reinterpret_cast<uint32_t*>(wsm + kDecSlotTable);       // u32[256]: f | cum << 16
+    uint32_t* plist = reinterpret_cast<uint32_t*>(wsm + kDecSlotTable + 1024); // u32[256]: cum << 8 | s
+    if (len < kStreamHead) return false;
+    uint32_t x = reinterpret_cast<const uint32_t*>(src)[lane];
+    const uint32_t bm = src[128 + lane];  // present symbols 8*lane .. 8*lane+7
+    uint32_t k_total;
+    const uint32_t prefix = warp_excl_scan_d(__popc(bm), lane, &k_total);
+    if (len < kStreamHead + 2 * k_total || ((len - kStreamHead - 2 * k_total) & 1u)) return false;
+    const uint32_t W = (len - kStreamHead - 2 * k_total) / 2;
+    uint32_t f[8];
+    uint32_t lsum = 0;
+    bool bad = x < kRansL;
+    {
+        uint32_t idx = prefix;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            f[k] = 0;
+            if (bm & (1u << k)) {
+                f[k] = reinterpret_cast<const uint16_t*>(src + kStreamHead)[idx++];
+                if (f[k] == 0 || f[k] > kM) bad = true;
+            }
+            lsum += f[k];
+        }
+    }
+    uint32_t fsum;
+    uint32_t cum = warp_excl_scan_d(lsum, lane, &fsum);
+    if (__any_sync(0xFFFFFFFFu, bad) || fsum != kM) return false;
+    {
+        uint32_t idx = prefix;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (bm & (1u << k)) {
+                sym_fc[8 * lane + k] = f[k] | (cum << 16);
+                plist[idx++] = (cum << 8) | (8 * lane + k);
+            }
+            cum += f[k];
+        }
+    }
+    __syncwarp();
+    // slot table: lane fills slots [128 lane, 128 lane + 128)
+    {
+        const uint32_t first = 128 * lane;
+        // largest j with cum_j <= first (binary search over the sorted list)
+        uint32_t lo = 0, hi = k_total - 1;
+        while (lo < hi) {
+            const uint32_t mid = (lo + hi + 1) / 2;
+            if ((plist[mid] >> 8) <= first) lo = mid;
+            else hi = mid - 1;
+        }
+        uint32_t j = lo;
+        uint32_t cur = plist[j] & 0xFFu;
+        uint32_t next_cum = j + 1 < k_total ? (plist[j + 1] >> 8) : kM;
+        for (uint32_t g = 0; g < 32; ++g) {
+            const uint32_t i0 = first + 4 * g;
+            uint32_t word;
+            if (next_cum > i0 + 3) {
+                word = cur * 0x01010101u;
+            } else {
+                word = 0;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    while (next_cum <= i0 + b) {
+                        ++j;
+                        cur = plist[j] & 0xFFu;
+                        next_cum = j + 1 < k_total ? (plist[j + 1] >> 8) : kM;
+                    }
+                    word |= cur << (8 * b);
+                }
+            }
+            reinterpret_cast<uint32_t*>(slot_sym)[i0 / 4] = word;
+        }
+    }
+    __syncwarp();
+
+    const uint16_t* words = reinterpret_cast<const uint16_t*>(src + kStreamHead + 2 * k_total);
+    const uint32_t lt = lanemask_lt();
+    uint32_t pos = 0;
+    const uint32_t T = (n_c + 31) / 32;
+    auto step = [&](uint32_t t, uint32_t r, bool active) {
+        const uint32_t slot = x & (kM - 1);
+        const uint32_t s = slot_sym[slot];
+        const uint32_t fc = sym_fc[s];
+        uint32_t xn = (fc & 0xFFFFu) * (x >> kProbBits) + slot - (fc >> 16);
+        const bool need = active && xn < kRansL;
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, need);
+        if (need) {
+            const uint32_t wi = pos + __popc(b & lt);
+            uint32_t w = 0;
+            if (wi < W) w = words[wi];
+            else bad = true;
+            xn = (xn << 16) | w;
+        }
+        pos += __popc(b);
+        if (active) {
+            x = xn;
+            const uint32_t v = merge_bits<DT>(s, r);
+            const uint64_t i = 32 * uint64_t(t) + lane;
+            if (es == 2) reinterpret_cast<uint16_t*>(out)[i] = uint16_t(v);
+            else reinterpret_cast<uint32_t*>(out)[i] = v;
+        }
+    };
+    auto load_rem = [&](uint32_t t) -> uint32_t {
+        const uint32_t i = 32 * t + lane;
+        if (i >= n_c) return 0;
+        if (DT == UZIP_BF16) return rem[i];
+        return uint32_t(rem[3 * uint64_t(i)]) | uint32_t(rem[3 * uint64_t(i) + 1]) << 8 |
+               uint32_t(rem[3 * uint64_t(i) + 2]) << 16;
+    };
+    if (n_c == kChunk) {
+        uint32_t ra[16], rbk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ra[j] = load_rem(j);
+        for (uint32_t t0 = 0; t0 < kSteps; t0 += 32) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) rbk[j] = load_rem(t0 + 16 + j);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) step(t0 + j, ra[j], true);
+            if (t0 + 32 < kSteps) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) ra[j] = load_rem(t0 + 32 + j);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) step(t0 + 16 + j, rbk[j], true);
+        }
+    } else {
+        for (uint32_t t = 0; t < T; ++t) step(t, load_rem(t), 32 * t + lane < n_c);
+    }
+    const bool fail = bad || x != kRansL || pos != W;
+    return !__any_sync(0xFFFFFFFFu, fail);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kDecWarps * 32) decompress_kernel(DecompressArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t wid = threadIdx.x >> 5;
+    uint8_t* wsm = smem + wid * kDecWarpSmem;
+    constexpr uint32_t es = DT == UZIP_BF16 ? 2 : 4;
+    constexpr uint32_t rb = DT == UZIP_BF16 ? 1 : 3;
+    const uint8_t* h = a.comp;
+    const uint64_t n = a.n;
+    const uint64_t C = num_chunks(n);
+    const uint64_t rem_off = rem_offset(n);
+    const uint64_t exp_off = exp_offset(DT, n);
+    // header checks (every warp, broadcast loads)
+    const uint64_t total = *reinterpret_cast<const uint64_t*>(h + 40);
+    bool ok = *reinterpret_cast<const uint32_t*>(h) == 0x31505A55u && *reinterpret_cast<const uint16_t*>(h + 4) == 1 &&
+              h[6] == uint8_t(DT) && h[7] == 0 && *reinterpret_cast<const uint64_t*>(h + 8) == n &&
+              *reinterpret_cast<const uint32_t*>(h + 16) == kChunk && *reinterpret_cast<const uint32_t*>(h + 20) == C &&
+              *reinterpret_cast<const uint64_t*>(h + 24) == rem_off &&
+              *reinterpret_cast<const uint64_t*>(h + 32) == exp_off && total <= a.cap && total >= exp_off;
+    if (!ok) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag_corrupt(a.status);
+        return;
+    }
+    const uint64_t section = total - exp_off;
+    const uint64_t nwarps = uint64_t(gridDim.x) * kDecWarps;
+    for (uint64_t c = uint64_t(blockIdx.x) * kDecWarps + wid; c < C; c += nwarps) {
+        const uint64_t off = reinterpret_cast<const uint64_t*>(h + kHeader)[c];
+        const uint32_t lw = reinterpret_cast<const uint32_t*>(h + kHeader + 8 * C)[c];
+        const bool raw = (lw & kRawFlag) != 0;
+        const uint32_t len = lw & ~kRawFlag;
+        const uint64_t left = n - c * kChunk;
+        const uint32_t n_c = uint32_t(left < kChunk ? left : kChunk);
+        bool good = (off & 15u) == 0 && off <= section && len <= section - off;
+        if (good) {
+            const uint8_t* src = h + exp_off + off;
+            const uint8_t* rem = h + rem_off + c * kChunk * rb;
+            uint8_t* out = a.out + c * kChunk * es;
+            if (raw) {
+                if (len == n_c) merge_raw<DT>(src, rem, out, n_c, lane);
+                else good = false;
+            } else {
+                good = decode_coded<DT>(src, len, rem, out, n_c, lane, wsm);
+            }
+        }
+        if (!good && lane == 0) flag_corrupt(a.status);
+        __syncwarp();
+    }
+}
+
+cudaError_t launch_decompress(int dtype, const void* d_comp, uint64_t cap, void* d_out, uint64_t n, int32_t* d_status,
+                              cudaStream_t s) {
+    cudaError_t err;
+    if (d_status && (err = cudaMemsetAsync(d_status, 0, sizeof(int32_t), s)) != cudaSuccess) return err;
+    DecompressArgs a{static_cast<const uint8_t*>(d_comp), cap, static_cast<uint8_t*>(d_out), n, d_status};
+    const uint64_t C = num_chunks(n);  // C == 0 still launches one block to validate the header
+    int dev = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    int sms = 0;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    void (*kern)(DecompressArgs) = dtype == UZIP_BF16 ? decompress_kernel<UZIP_BF16> : decompress_kernel<UZIP_FP32>;
+    const uint32_t smem = kDecWarps * kDecWarpSmem;
+    int per_sm = 0;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecWarps * 32, smem)) != cudaSuccess)
+        return err;
+    if (per_sm < 1) per_sm = 1;
+    uint64_t grid = uint64_t(per_sm) * uint64_t(sms);
+    const uint64_t need = (C + kDecWarps - 1) / kDecWarps;
+    if (grid > need) grid = need;
+    if (grid < 1) grid = 1;
+    kern<<<dim3(uint32_t(grid)), dim3(kDecWarps * 32), smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace uzip

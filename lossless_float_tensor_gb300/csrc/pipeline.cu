@@ -1,0 +1,111 @@
+// Split-send pipeline on one GPU (UCCL-Zip Fig. 1 b and Fig. 4 d: expose
+// transmissible data early and overlap the transfer with the remaining
+// compression; NCCLZ Sec. IV-D4: two ping-pong staging banks, batch i+1 is
+// encoded into one bank while batch i is in flight from the other).  The
+// device-to-host copy into pinned memory stands in for the wire.
+#include "uzip_internal.cuh"
+
+namespace uzip {
+
+// Copies exactly total_bytes (read from the container header on the device)
+// into mapped host memory with 16-byte stores.  total_bytes is a multiple of
+// 16 for every container the compressor writes; a failed compression has
+// total_bytes = 0 and copies nothing.
+__global__ void copy_exact_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst) {
+    const uint64_t total = *reinterpret_cast<const volatile uint64_t*>(src + 40);
+    const uint64_t nvec = total / 16;
+    const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+    for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride)
+        reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+}
+
+cudaError_t launch_copy_exact(const void* d_container, void* h_dst_mapped, cudaStream_t s) {
+    int dev = 0, sms = 0;
+    cudaError_t err;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    copy_exact_kernel<<<dim3(uint32_t(sms) * 2), dim3(512), 0, s>>>(static_cast<const uint8_t*>(d_container),
+                                                                      static_cast<uint8_t*>(h_dst_mapped));
+    return cudaGetLastError();
+}
+
+}  // namespace uzip
+
+namespace {
+bool host_mapped(const void* p, void** dev) {
+    cudaPointerAttributes attr;
+    if (p == nullptr || cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return false;
+    if (dev) *dev = attr.devicePointer;
+    return true;
+}
+}  // namespace
+
+extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d_msgs, const uint64_t* msg_elems,
+                                          uint32_t n_msgs, void* const* d_bank, uint64_t bank_capacity,
+                                          void* const* h_bank, uint64_t h_capacity, uint64_t* h_sizes,
+                                          uzip_pipe_mode mode, cudaStream_t s_compress, cudaStream_t s_copy) {
+    using namespace uzip;
+    if (dtype != UZIP_BF16 && dtype != UZIP_FP32) return UZIP_ERR_UNSUPPORTED_DTYPE;
+    if (n_msgs == 0 || !d_msgs || !msg_elems || !d_bank || !h_bank || !h_sizes) return UZIP_ERR_INVALID_ARG;
+    if (mode != UZIP_PIPE_EXACT && mode != UZIP_PIPE_BOUND && mode != UZIP_PIPE_SERIAL) return UZIP_ERR_INVALID_ARG;
+    uint64_t largest = 0;
+    for (uint32_t k = 0; k < n_msgs; ++k) {
+        if (msg_elems[k] > UZIP_MAX_ELEMS) return UZIP_ERR_INVALID_ARG;
+        if (msg_elems[k] > largest) largest = msg_elems[k];
+    }
+    if (bank_capacity < uzip_max_compressed_size(dtype, largest)) return UZIP_ERR_CAPACITY;
+    if (h_capacity < container_bound(dtype, largest)) return UZIP_ERR_CAPACITY;
+    void* h_dev[2] = {nullptr, nullptr};
+    void* sizes_dev = nullptr;
+    for (int b = 0; b < 2; ++b) {
+        if (!d_bank[b] || (reinterpret_cast<uintptr_t>(d_bank[b]) & 15)) return UZIP_ERR_INVALID_ARG;
+        if (!host_mapped(h_bank[b], &h_dev[b]) || (reinterpret_cast<uintptr_t>(h_dev[b]) & 15))
+            return UZIP_ERR_INVALID_ARG;
+    }
+    if (d_bank[0] == d_bank[1] || h_bank[0] == h_bank[1]) return UZIP_ERR_INVALID_ARG;
+    if (!host_mapped(h_sizes, &sizes_dev) || (reinterpret_cast<uintptr_t>(sizes_dev) & 7)) return UZIP_ERR_INVALID_ARG;
+
+    const bool serial = mode == UZIP_PIPE_SERIAL;
+    cudaStream_t sc = s_compress;
+    cudaStream_t sx = serial ? s_compress : s_copy;
+    cudaEvent_t compressed[2] = {nullptr, nullptr}, copied[2] = {nullptr, nullptr};
+    uzip_status result = UZIP_OK;
+    for (int b = 0; b < 2 && result == UZIP_OK; ++b) {
+        if (cudaEventCreateWithFlags(&compressed[b], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&copied[b], cudaEventDisableTiming) != cudaSuccess)
+            result = UZIP_ERR_CUDA;
+    }
+    for (uint32_t k = 0; k < n_msgs && result == UZIP_OK; ++k) {
+        const int b = int(k & 1u);
+        // bank b still holds message k-2 until its copy has finished
+        if (k >= 2 && !serial && cudaStreamWaitEvent(sc, copied[b], 0) != cudaSuccess) {
+            result = UZIP_ERR_CUDA;
+            break;
+        }
+        result = uzip_compress(d_msgs[k], dtype, msg_elems[k], d_bank[b], bank_capacity,
+                               static_cast<uint64_t*>(sizes_dev) + k, sc);
+        if (result != UZIP_OK) break;
+        if (!serial && (cudaEventRecord(compressed[b], sc) != cudaSuccess ||
+                        cudaStreamWaitEvent(sx, compressed[b], 0) != cudaSuccess)) {
+            result = UZIP_ERR_CUDA;
+            break;
+        }
+        cudaError_t err;
+        if (mode == UZIP_PIPE_BOUND)
+            err = cudaMemcpyAsync(h_bank[b], d_bank[b], container_bound(dtype, msg_elems[k]), cudaMemcpyDeviceToHost, sx);
+        else
+            err = launch_copy_exact(d_bank[b], h_dev[b], sx);
+        if (err == cudaSuccess && !serial) err = cudaEventRecord(copied[b], sx);
+        if (err != cudaSuccess) result = UZIP_ERR_CUDA;
+    }
+    for (int b = 0; b < 2; ++b) {
+        if (compressed[b]) cudaEventDestroy(compressed[b]);
+        if (copied[b]) cudaEventDestroy(copied[b]);
+    }
+    if (result == UZIP_ERR_CUDA) cudaGetLastError();
+    return result;
+}

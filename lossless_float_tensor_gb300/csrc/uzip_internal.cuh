@@ -1,0 +1,174 @@
+// Internal definitions shared by the uzip CUDA sources: container layout,
+// launch constants and small inline-PTX helpers.  Nothing here is exported.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/uzip.h"
+
+namespace uzip {
+
+// ---- container format (see include/uzip.h) --------------------------------
+constexpr uint32_t kChunk = 65536;        // elements per chunk
+constexpr uint32_t kLanes = 32;           // interleaved rANS states
+constexpr uint32_t kSteps = kChunk / kLanes;
+constexpr uint32_t kProbBits = 12;
+constexpr uint32_t kM = 1u << kProbBits;  // frequency total 4096
+constexpr uint32_t kRansL = 1u << 16;     // state interval [2^16, 2^32)
+constexpr uint32_t kHeader = 64;
+constexpr uint32_t kRawFlag = 0x80000000u;
+constexpr uint32_t kStreamHead = 160;     // 32 states + 32-byte bitmap
+
+__host__ __device__ inline uint64_t round16(uint64_t v) { return (v + 15) & ~uint64_t(15); }
+__host__ __device__ inline uint32_t rem_bytes(int dtype) { return dtype == UZIP_BF16 ? 1u : 3u; }
+__host__ __device__ inline uint32_t elem_bytes(int dtype) { return dtype == UZIP_BF16 ? 2u : 4u; }
+__host__ __device__ inline uint64_t num_chunks(uint64_t n) { return (n + kChunk - 1) / kChunk; }
+__host__ __device__ inline uint64_t rem_offset(uint64_t n) { return round16(kHeader + 12 * num_chunks(n)); }
+__host__ __device__ inline uint64_t exp_offset(int dtype, uint64_t n) {
+    return round16(rem_offset(n) + n * rem_bytes(dtype));
+}
+// Largest container: every chunk stored RAW (round16 of each chunk length).
+__host__ __device__ inline uint64_t container_bound(int dtype, uint64_t n) {
+    uint64_t c = num_chunks(n);
+    uint64_t body = 0;
+    if (c > 0) body = (c - 1) * uint64_t(kChunk) + round16(n - (c - 1) * uint64_t(kChunk));
+    return exp_offset(dtype, n) + body;
+}
+
+// ---- compressor work area, placed at round16(container_bound) in d_out ----
+struct Scratch {
+    uint32_t status;      // 0 or a uzip_status set by the first failing chunk
+    uint32_t ticket;      // next chunk to take
+    uint32_t done;        // chunks finished
+    uint32_t pad;
+    // followed by uint64_t desc[C]: decoupled look-back descriptors
+};
+constexpr uint64_t kScratchHead = 16;
+__host__ __device__ inline uint64_t scratch_offset(int dtype, uint64_t n) { return round16(container_bound(dtype, n)); }
+__host__ __device__ inline uint64_t scratch_bytes(uint64_t n) { return kScratchHead + 8 * num_chunks(n); }
+
+// look-back descriptor: flag in bits 62..63, byte count in bits 0..61
+constexpr uint64_t kDescAggregate = 1ull << 62;
+constexpr uint64_t kDescInclusive = 2ull << 62;
+constexpr uint64_t kDescValue = (1ull << 62) - 1;
+
+// ---- compressor shared-memory plan (one warp per CTA) ---------------------
+// region A (32 KiB): phase 1 lane-private histogram u32[256][32];
+//                    phase 2 encode table (4 KiB) then word staging.
+// region B (2 KiB) : counts, frequencies, bitmap, present-symbol list.
+constexpr uint32_t kRegionA = 32768;
+constexpr uint32_t kEncTable = 4096;        // 256 x 16 bytes
+constexpr uint32_t kStageBase = kEncTable;  // staging occupies [kStageBase, kRegionA)
+constexpr uint32_t kRegionB = 2048;
+constexpr uint32_t kCompressSmem = kRegionA + kRegionB;
+
+// spin limit of a look-back wait: iterations with a growing back-off (about a
+// second of waiting in total)
+constexpr uint32_t kSpinLimit = 1u << 20;
+
+// ---- decompressor shared-memory plan (per warp) ---------------------------
+constexpr uint32_t kDecWarps = 4;
+constexpr uint32_t kDecSlotTable = 4096;    // slot -> symbol, u8[4096]
+constexpr uint32_t kDecSymTable = 1024;     // symbol -> f | cum << 16, u32[256]
+constexpr uint32_t kDecList = 1024;         // present symbols, u32[256]: cum << 8 | symbol
+constexpr uint32_t kDecWarpSmem = kDecSlotTable + kDecSymTable + kDecList;
+
+// ---- inline PTX helpers ----------------------------------------------------
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_v4_hint(const void* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_u16_hint(const void* p, uint64_t pol) {
+    unsigned short v;
+    asm volatile("ld.global.nc.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_u32_hint(const void* p, uint64_t pol) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void st_v2_hint(void* p, uint32_t a, uint32_t b, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1,%2}, %3;" ::"l"(p), "r"(a), "r"(b), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_u32_hint(void* p, uint32_t a, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(p), "r"(a), "l"(pol) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Exact floor(x / f) for x in [16 f, f * 2^20) as (x * m + add) >> (32 + sh)
+// (Robison, "N-bit unsigned division via N-bit multiply-add", ARITH 2005).
+// With p = max(32, 31 + ceil(log2 f)) the reciprocal fits 32 bits; either the
+// round-up reciprocal (add = 0) or the round-down reciprocal with increment
+// (add = m) is exact over the whole range.  Exactness reduces to the worst
+// points x = k f - 1 (round-up: (f 2^20 - 1) e < 2^p, e = m f - 2^p) and
+// x = k f (round-down: ((2^20 - 1) f + 1) d <= 2^p, d = 2^p - m f); one of the
+// two holds for every f in [1, 4096] (checked exhaustively by the tests
+// through uzip_debug_div_magic).
+struct DivMagic {
+    uint32_t m, add, sh, ok;
+};
+__host__ __device__ inline DivMagic div_magic(uint32_t f) {
+    DivMagic r{0u, 0u, 0u, 0u};
+    if (f == 0 || f > kM) return r;
+    uint32_t lg = 0;
+    while ((1u << lg) < f) ++lg;  // ceil(log2 f)
+    const uint32_t p = lg + 31 < 32 ? 32 : lg + 31;
+    const uint64_t two_p = 1ull << p;
+    const uint64_t md = (two_p - 1) / f;  // floor((2^p - 1) / f)
+    const uint64_t mu = md + 1;           // ceil(2^p / f)
+    const uint64_t xmax = (uint64_t(f) << 20) - 1;
+    r.sh = p - 32;
+    if (mu < (1ull << 32)) {
+        const uint64_t e = mu * f - two_p;
+        if (xmax * e < two_p) {
+            r.m = uint32_t(mu);
+            r.add = 0;
+            r.ok = 1;
+            return r;
+        }
+    }
+    const uint64_t d = two_p - md * f;
+    if (md < (1ull << 32) && (((1ull << 20) - 1) * f + 1) * d <= two_p) {
+        r.m = uint32_t(md);
+        r.add = uint32_t(md);
+        r.ok = 1;
+    }
+    return r;
+}
+
+// launchers (compress.cu, decompress.cu, pipeline.cu)
+cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
+                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s);
+cudaError_t launch_decompress(int dtype, const void* d_comp, uint64_t cap, void* d_out, uint64_t n, int32_t* d_status,
+                              cudaStream_t s);
+cudaError_t launch_copy_exact(const void* d_container, void* h_dst_mapped, cudaStream_t s);
+
+}  // namespace uzip

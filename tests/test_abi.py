@@ -1,0 +1,102 @@
+"""Host-side checks of the C-ABI library: it loads without a GPU, exports every
+symbol its headers declare, and its host-only arithmetic is right."""
+import os
+import random
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(uzip_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def uz():
+    import __graft_entry__
+
+    __graft_entry__.build_library()
+    import lossless_float_tensor_gb300 as uz
+
+    return uz
+
+
+def test_exports_every_declared_symbol(uz):
+    names = _declared_functions()
+    assert {"uzip_max_compressed_size", "uzip_compress", "uzip_decompress", "uzip_query_size"} <= names
+    lib = uz.library()
+    for name in sorted(names):
+        assert hasattr(lib, name), name
+
+
+def test_max_compressed_size_is_container_bound_plus_work_area(uz):
+    for dtype in (0, 1):
+        for n in [0, 1, 15, 16, 17, 65535, 65536, 65537, 3 * 65536 + 5, 1 << 29]:
+            c = -(-n // 65536)
+            bound = oracle.container_bound(dtype, n)
+            off = uz.library().uzip_debug_scratch_offset(dtype, n)
+            assert off == -(-bound // 16) * 16
+            assert uz.uzip_max_compressed_size(dtype, n) == off + 16 + 8 * c
+    assert uz.uzip_max_compressed_size(7, 10) == 0
+    assert uz.uzip_max_compressed_size(0, (1 << 40) + 1) == 0
+
+
+def test_division_magic_exact_for_every_frequency(uz):
+    """x // f == (x*m + add) >> shift for x in [16f, f*2^20): the worst cases
+    x = k f - 1 and x = k f at the top of the range, the bottom, and random x."""
+    import ctypes
+
+    lib = uz.library()
+    m, add, sh = ctypes.c_uint32(), ctypes.c_uint32(), ctypes.c_uint32()
+    rng = random.Random(7)
+    for f in range(1, 4097):
+        assert lib.uzip_debug_div_magic(f, ctypes.byref(m), ctypes.byref(add), ctypes.byref(sh)) == 1
+        M, A, S = m.value, add.value, sh.value
+        assert A in (0, M) and 32 <= S <= 44
+        top = f << 20
+        xs = {16 * f, 16 * f + 1, top - 1, top - f, top - f - 1, top - 2 * f, top - 2 * f + 1}
+        xs |= {rng.randrange(16 * f, top) for _ in range(24)}
+        for x in xs:
+            assert (x * M + A) >> S == x // f, (f, x)
+        # closed-form exactness over the whole range
+        two_p = 1 << S
+        if A == 0:
+            assert (top - 1) * (M * f - two_p) < two_p
+        else:
+            assert (((1 << 20) - 1) * f + 1) * (two_p - M * f) <= two_p
+    assert lib.uzip_debug_div_magic(0, None, None, None) == 0
+    assert lib.uzip_debug_div_magic(4097, None, None, None) == 0
+
+
+def test_status_strings(uz):
+    assert uz.uzip_status_string(0) == "ok"
+    assert uz.uzip_status_string(4) == "corrupt container"
+    assert uz.uzip_status_string(99) == "unknown status"
+
+
+def test_host_argument_checks(uz):
+    """Rejected on the host before any CUDA call."""
+    fake = 1 << 40  # aligned, never dereferenced
+    assert uz.uzip_compress(fake, 5, 10, fake, 1 << 20, None, 0) == uz.UZIP_ERR_UNSUPPORTED_DTYPE
+    assert uz.uzip_compress(None, 0, 10, fake, 1 << 20, None, 0) == uz.UZIP_ERR_INVALID_ARG
+    assert uz.uzip_compress(fake + 8, 0, 10, fake, 1 << 20, None, 0) == uz.UZIP_ERR_INVALID_ARG
+    assert uz.uzip_compress(fake, 0, 10, None, 1 << 20, None, 0) == uz.UZIP_ERR_INVALID_ARG
+    assert uz.uzip_compress(fake, 0, 10, fake, 100, None, 0) == uz.UZIP_ERR_CAPACITY
+    assert uz.uzip_compress(fake, 0, (1 << 40) + 1, fake, 1 << 20, None, 0) == uz.UZIP_ERR_INVALID_ARG
+    assert uz.uzip_compress_ex(fake, 0, 10, fake, 1 << 20, None, None, 8, 0) == uz.UZIP_ERR_INVALID_ARG
+    assert uz.uzip_decompress(fake, 32, fake, 0, 10, None, 0) == uz.UZIP_ERR_CORRUPT
+    assert uz.uzip_decompress(None, 1 << 20, fake, 0, 10, None, 0) == uz.UZIP_ERR_INVALID_ARG
+    assert uz.uzip_decompress(fake, 1 << 20, fake, 3, 10, None, 0) == uz.UZIP_ERR_UNSUPPORTED_DTYPE
+    assert uz.uzip_query_size(None, 0)[0] == uz.UZIP_ERR_INVALID_ARG
