@@ -141,7 +141,7 @@ def run_ours(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    bits = synth.c4()
+    bits = synth.c4(n=args.elements)
     n = bits.size
     x = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
     cap = uz.uzip_max_compressed_size(uz.UZIP_BF16, n)
@@ -197,7 +197,9 @@ def run_ours(args, rank, world, local_rank):
     value = world * in_bytes * args.steps / (dev_ms / 1e3) / 1e9
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(args, x, bits, comp, cap, size, out, status, stream, dev, total) if rank == 0 else None
+    e2e = None
+    if rank == 0 and not args.no_e2e:
+        e2e = run_e2e(args, x, bits, comp, cap, size, out, status, stream, dev, total)
 
     if rank != 0:
         return None
@@ -219,7 +221,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "elements": n, "input_bytes": in_bytes, "parallelism": f"replicas x{world}",
+        "config": {"workload": WORKLOAD if args.elements is None else f"first {n} values of " + WORKLOAD,
+                   "elements": n, "input_bytes": in_bytes, "parallelism": f"replicas x{world}",
                    "l2": "inputs (1 GiB) larger than L2; no flush"},
         "compress_gbs": in_bytes / (mc / 1e3) / 1e9, "decompress_gbs": in_bytes / (md / 1e3) / 1e9,
         "ratio": total / in_bytes, "compressed_bytes": total,
@@ -325,6 +328,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--elements", type=int, default=None,
+                    help="use only the first N values of the workload (profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
