@@ -59,7 +59,8 @@ typedef enum {
     UZIP_ERR_CAPACITY = 3,          /* output buffer smaller than required */
     UZIP_ERR_CORRUPT = 4,           /* container failed validation */
     UZIP_ERR_TIMEOUT = 5,           /* a bounded device-side wait ran out */
-    UZIP_ERR_CUDA = 6               /* a CUDA runtime call or launch failed */
+    UZIP_ERR_CUDA = 6,              /* a CUDA runtime call or launch failed */
+    UZIP_ERR_TOO_LARGE = 7          /* n above UZIP_NOALLOC_MAX_ELEMS (uzip_compress_noalloc) */
 } uzip_status;
 
 /* Largest number of elements one call accepts (2^40). */
@@ -97,6 +98,36 @@ uzip_status uzip_compress(const void* d_in, uzip_dtype dtype, uint64_t n, void* 
 uzip_status uzip_compress_ex(const void* d_in, uzip_dtype dtype, uint64_t n, void* d_out,
                              uint64_t out_capacity, uint64_t* d_out_size, int32_t* d_status,
                              uint32_t flags, cudaStream_t s);
+
+/* Allocation-free compression.  The pages have no counterpart: this entry
+ * point serves callers that hold only the user's input and output buffers and
+ * must not allocate device memory of their own -- for instance a transport or
+ * plugin hook that runs once per message inside someone else's memory plan,
+ * where a cudaMalloc could stall the whole device and would take memory the
+ * application has budgeted elsewhere.  uzip_compress needs a small work area
+ * (16 + 8 * ceil(n / 65536) bytes) at the tail of its output buffer; this
+ * variant keeps that work area in the library's own device memory instead: a
+ * fixed array in the library, one per GPU that loads it, kept until the
+ * process exits.
+ *
+ *   d_in, n, dtype   as uzip_compress; n <= UZIP_NOALLOC_MAX_ELEMS (2^30,
+ *                    so the array is 131,088 bytes), else UZIP_ERR_TOO_LARGE.
+ *   d_out            device, 16-byte aligned; out_capacity must be at least
+ *                    the largest container, uzip_max_compressed_size(dtype, n)
+ *                    - 16 - 8 * ceil(n / 65536) bytes (else UZIP_ERR_CAPACITY).
+ *   d_out_size, d_status  as uzip_compress_ex (both nullable).
+ * The result is byte for byte the container uzip_compress writes.  The call
+ * allocates nothing: it clears the work area with cudaMemsetAsync on s and
+ * launches the same kernel.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  Every call shares the one array, so
+ * two calls whose work overlaps on the GPU (different streams, or different
+ * host threads without ordering) race and corrupt each other's output: order
+ * them on one stream or synchronise between them. */
+#define UZIP_NOALLOC_MAX_ELEMS (1ull << 30)
+uzip_status uzip_compress_noalloc(const void* d_in, uzip_dtype dtype, uint64_t n, void* d_out,
+                                  uint64_t out_capacity, uint64_t* d_out_size, int32_t* d_status,
+                                  cudaStream_t s);
 
 /* Decompress the container at d_comp into n elements at d_out.
  *   d_comp         device, 16-byte aligned; comp_capacity = readable bytes

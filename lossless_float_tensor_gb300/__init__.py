@@ -23,6 +23,8 @@ UZIP_ERR_CAPACITY = 3
 UZIP_ERR_CORRUPT = 4
 UZIP_ERR_TIMEOUT = 5
 UZIP_ERR_CUDA = 6
+UZIP_ERR_TOO_LARGE = 7
+UZIP_NOALLOC_MAX_ELEMS = 1 << 30
 UZIP_TESTFLAG_SKIP_CHUNK0 = 1
 UZIP_PIPE_EXACT, UZIP_PIPE_BOUND, UZIP_PIPE_SERIAL = 0, 1, 2
 UZIP_MAX_ELEMS = 1 << 40
@@ -41,6 +43,8 @@ _lib.uzip_compress.argtypes = [_vp, _int, _u64, _vp, _u64, _vp, _vp]
 _lib.uzip_compress.restype = _int
 _lib.uzip_compress_ex.argtypes = [_vp, _int, _u64, _vp, _u64, _vp, _vp, _u32, _vp]
 _lib.uzip_compress_ex.restype = _int
+_lib.uzip_compress_noalloc.argtypes = [_vp, _int, _u64, _vp, _u64, _vp, _vp, _vp]
+_lib.uzip_compress_noalloc.restype = _int
 _lib.uzip_decompress.argtypes = [_vp, _u64, _vp, _int, _u64, _vp, _vp]
 _lib.uzip_decompress.restype = _int
 _lib.uzip_query_size.argtypes = [_vp, ctypes.POINTER(_u64), ctypes.POINTER(_int), ctypes.POINTER(_u64), _vp]
@@ -75,6 +79,14 @@ def uzip_compress(d_in: int, dtype: int, n: int, d_out: int, out_capacity: int, 
 def uzip_compress_ex(d_in: int, dtype: int, n: int, d_out: int, out_capacity: int, d_out_size: int | None,
                      d_status: int | None, flags: int, stream: int) -> int:
     return int(_lib.uzip_compress_ex(d_in, dtype, n, d_out, out_capacity, d_out_size, d_status, flags, stream))
+
+
+def uzip_compress_noalloc(d_in: int, dtype: int, n: int, d_out: int, out_capacity: int, d_out_size: int | None,
+                          d_status: int | None, stream: int) -> int:
+    """Compression that allocates nothing: the work area is the library's own
+    device array (tensors up to UZIP_NOALLOC_MAX_ELEMS values; calls sharing a
+    GPU must not overlap)."""
+    return int(_lib.uzip_compress_noalloc(d_in, dtype, n, d_out, out_capacity, d_out_size, d_status, stream))
 
 
 def uzip_decompress(d_comp: int, comp_capacity: int, d_out: int, dtype: int, n: int, d_status: int | None,

@@ -15,6 +15,8 @@
 // A chunk whose stream does not fit the staging area is re-encoded twice
 // (count, then write in place); a chunk that coding does not shrink is stored
 // RAW (NCCLZ Sec. IV-C).
+#include <mutex>
+
 #include "uzip_internal.cuh"
 
 namespace uzip {
@@ -662,12 +664,16 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// host launcher (called by the C ABI after argument checks)
-cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
-                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s) {
+// host launchers (called by the C ABI after argument checks)
+
+// Launches the compressor with its work area (status, ticket, done counter,
+// look-back descriptors: scratch_bytes(n) bytes) at `scratch`, which is
+// zeroed on `s` first.
+cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
+                                         int32_t* d_status, uint32_t first_ticket, void* scratch_area, cudaStream_t s) {
     const uint64_t C = num_chunks(n);
     uint8_t* out = static_cast<uint8_t*>(d_out);
-    Scratch* scratch = reinterpret_cast<Scratch*>(out + scratch_offset(dtype, n));
+    Scratch* scratch = static_cast<Scratch*>(scratch_area);
     cudaError_t err = cudaMemsetAsync(scratch, 0, scratch_bytes(n), s);
     if (err != cudaSuccess) return err;
     CompressArgs a;
@@ -695,6 +701,46 @@ cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out
     if (grid < 1) grid = 1;
     kern<<<dim3(uint32_t(grid)), dim3(32), kCompressSmem, s>>>(a);
     return cudaGetLastError();
+}
+
+// The regular path: the work area sits in the caller's output buffer, behind
+// the largest possible container.
+cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
+                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s) {
+    uint8_t* out = static_cast<uint8_t*>(d_out);
+    return launch_compress_with_scratch(dtype, d_in, n, d_out, d_out_size, d_status, first_ticket,
+                                        out + scratch_offset(dtype, n), s);
+}
+
+// ---------------------------------------------------------------------------
+// Work area for callers that may not allocate device memory (see
+// uzip_compress_noalloc).  It lives in the library's own module memory, one
+// copy per GPU that loads the library, held until the process exits, and is
+// sized for kNoAllocMaxElems elements.  Every call shares it.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchHead + 8 * (kNoAllocMaxElems / kChunk)];
+
+namespace {
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+}  // namespace
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name only stands in for the symbol, so the address is asked of
+// the runtime once per device (with that device current) and cached.
+cudaError_t noalloc_scratch_address(void** ptr) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= int(kNoAllocMaxDevices)) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (err != cudaSuccess) return err;
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return cudaSuccess;
 }
 
 }  // namespace uzip

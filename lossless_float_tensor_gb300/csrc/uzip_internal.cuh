@@ -167,6 +167,14 @@ __host__ __device__ inline DivMagic div_magic(uint32_t f) {
 // launchers (compress.cu, decompress.cu, pipeline.cu)
 cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                             int32_t* d_status, uint32_t first_ticket, cudaStream_t s);
+cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
+                                         int32_t* d_status, uint32_t first_ticket, void* scratch_area, cudaStream_t s);
+
+// allocation-free compression: largest tensor and device count served by the
+// library's own work area
+constexpr uint64_t kNoAllocMaxElems = 1ull << 30;
+constexpr uint32_t kNoAllocMaxDevices = 64;
+cudaError_t noalloc_scratch_address(void** ptr);
 cudaError_t launch_decompress(int dtype, const void* d_comp, uint64_t cap, void* d_out, uint64_t n, int32_t* d_status,
                               cudaStream_t s);
 cudaError_t launch_copy_exact(const void* d_container, void* h_dst_mapped, cudaStream_t s);
