@@ -83,42 +83,8 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
     uint8_t* hl = hist + lane4;
     constexpr uint32_t kPer = 16 / Traits<DT>::kEs;  // elements per 16-byte load
     const uint32_t nvec = n_c / kPer;
-    constexpr int U = 8;
-    uint32_t v = lane;
-    for (; v + 32 * (U - 1) < nvec; v += 32 * U) {
-        uint4 q[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) q[u] = ld_v4_hint(cin + uint64_t(v + 32 * u) * 16, pol_keep);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-            const uint32_t vi = v + 32 * u;
-            if (DT == UZIP_BF16) {
-                uint32_t r[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    r[j] = ((w[j] >> 8) & 0x00800080u) | (w[j] & 0x007F007Fu);
-                    atomicAdd(reinterpret_cast<uint32_t*>(hl + (w[j] & 0x7F80u)), 1u);
-                    atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
-                }
-                st_v2_hint(rem_dst + uint64_t(vi) * 8, __byte_perm(r[0], r[1], 0x6420), __byte_perm(r[2], r[3], 0x6420),
-                           pol_stream);
-            } else {
-                uint32_t r[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    r[j] = (w[j] & 0x7FFFFFu) | ((w[j] >> 8) & 0x800000u);
-                    atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
-                }
-                uint8_t* d = rem_dst + uint64_t(vi) * 12;
-                st_u32_hint(d, r[0] | (r[1] << 24), pol_stream);
-                st_u32_hint(d + 4, (r[1] >> 8) | (r[2] << 16), pol_stream);
-                st_u32_hint(d + 8, (r[2] >> 16) | (r[3] << 8), pol_stream);
-            }
-        }
-    }
-    for (; v < nvec; v += 32) {
-        uint4 q = ld_v4_hint(cin + uint64_t(v) * 16, pol_keep);
+    // one 16-byte vector: 8 bf16 or 4 fp32 values
+    auto process = [&](const uint4 q, uint32_t vi) {
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
         if (DT == UZIP_BF16) {
             uint32_t r[4];
@@ -128,7 +94,7 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
                 atomicAdd(reinterpret_cast<uint32_t*>(hl + (w[j] & 0x7F80u)), 1u);
                 atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
             }
-            st_v2_hint(rem_dst + uint64_t(v) * 8, __byte_perm(r[0], r[1], 0x6420), __byte_perm(r[2], r[3], 0x6420),
+            st_v2_hint(rem_dst + uint64_t(vi) * 8, __byte_perm(r[0], r[1], 0x6420), __byte_perm(r[2], r[3], 0x6420),
                        pol_stream);
         } else {
             uint32_t r[4];
@@ -137,12 +103,32 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
                 r[j] = (w[j] & 0x7FFFFFu) | ((w[j] >> 8) & 0x800000u);
                 atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
             }
-            uint8_t* d = rem_dst + uint64_t(v) * 12;
+            uint8_t* d = rem_dst + uint64_t(vi) * 12;
             st_u32_hint(d, r[0] | (r[1] << 24), pol_stream);
             st_u32_hint(d + 4, (r[1] >> 8) | (r[2] << 16), pol_stream);
             st_u32_hint(d + 8, (r[2] >> 16) | (r[3] << 8), pol_stream);
         }
+    };
+    // batches of U vectors per lane, two batches in flight
+    constexpr int U = 8;
+    const uint32_t nb = nvec / (32 * U);
+    uint4 qa[U], qb[U];
+    auto load = [&](uint4 (&q)[U], uint32_t k) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) q[u] = ld_v4_hint(cin + uint64_t(k * 32 * U + 32 * u + lane) * 16, pol_keep);
+    };
+    if (nb > 0) load(qa, 0);
+    for (uint32_t k = 0; k < nb; k += 2) {
+        if (k + 1 < nb) load(qb, k + 1);
+#pragma unroll
+        for (int u = 0; u < U; ++u) process(qa[u], k * 32 * U + 32 * u + lane);
+        if (k + 1 >= nb) break;
+        if (k + 2 < nb) load(qa, k + 2);
+#pragma unroll
+        for (int u = 0; u < U; ++u) process(qb[u], (k + 1) * 32 * U + 32 * u + lane);
     }
+    uint32_t v = nb * 32 * U + lane;
+    for (; v < nvec; v += 32) process(ld_v4_hint(cin + uint64_t(v) * 16, pol_keep), v);
     // ragged tail: element by element
     for (uint32_t i = nvec * kPer + lane; i < n_c; i += 32) {
         if (DT == UZIP_BF16) {
@@ -304,8 +290,24 @@ __device__ void build_enc_table(const Norm& nm, uint32_t lane, uint8_t* table, u
 }
 
 // ---------------------------------------------------------------------------
-// one rANS encode step for one lane (rule R6); returns the renormalisation
-// predicate.  entry = encode table row of the lane's symbol.
+// rANS encode (rule R6).  The table entry of a symbol is
+// {m, add, (f << 20) - 1, (M - f) | cum << 12 | sh << 27}.
+
+// Table loads are written as side-effect-free asm: the table does not change
+// while a chunk is encoded, so the compiler may issue them as early as it likes
+// (ahead of the staging stores of earlier steps).
+__device__ __forceinline__ uint4 lds_table(uint32_t saddr) {
+    uint4 v;
+    asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
+    return v;
+}
+__device__ __forceinline__ void sts_u16(uint32_t saddr, uint32_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(saddr), "h"(static_cast<unsigned short>(v)));
+}
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
 __device__ __forceinline__ uint32_t rans_update(uint32_t x, const uint4 e, bool emit) {
     const uint32_t xr = emit ? (x >> 16) : x;
     const uint32_t sh = e.w >> 27;
@@ -313,86 +315,164 @@ __device__ __forceinline__ uint32_t rans_update(uint32_t x, const uint4 e, bool 
     const uint32_t q = uint32_t(t >> 32) >> sh;
     const uint32_t mmf = e.w & 0xFFFu;
     const uint32_t cum = (e.w >> 12) & 0xFFFu;
-    return xr + q * mmf + cum;
+    return q * mmf + (xr + cum);
 }
 
 enum class Sink { Smem, Count, Global };
 
-// Encodes steps t = T-1 .. 0.  Sink::Smem stages words below *pos (u16 index
-// into region A) and returns false if the staging would pass `limit`;
-// Sink::Count only counts words and returns false once the coded length
-// reaches n_c (the chunk goes RAW); Sink::Global writes words to gwords in
-// place, *pos counting down from W.
+struct EncState {
+    uint32_t x;     // this lane's rANS state
+    int32_t pos;    // Smem: u16 index below which the next words go; Count: -words; Global: words left
+};
+
+// One encode step for one lane.  No branches: the word store is predicated.
 template <int DT, Sink S>
-__device__ bool encode_chunk(const uint8_t* __restrict__ cin, uint32_t n_c, const uint8_t* table, uint16_t* stage,
-                             uint32_t lane, uint32_t& x_out, int32_t& pos, int32_t limit, uint8_t* gwords,
-                             uint32_t hdr_bytes, uint64_t pol) {
+__device__ __forceinline__ void enc_step(EncState& st, uint32_t bits, bool active, uint32_t table_s, uint32_t stage_s,
+                                         uint8_t* gwords, uint32_t lt) {
+    const uint4 e = lds_table(table_s + Traits<DT>::table_off(bits));
+    const bool emit = active && (st.x > e.z);
+    const uint32_t b = __ballot_sync(0xFFFFFFFFu, emit);
+    const int32_t nt = __popc(b);
+    if (S == Sink::Smem) {
+        if (emit) sts_u16(stage_s + 2u * uint32_t(st.pos - nt + __popc(b & lt)), st.x);
+    } else if (S == Sink::Global) {
+        if (emit) *reinterpret_cast<uint16_t*>(gwords + 2 * uint64_t(uint32_t(st.pos - nt) + __popc(b & lt))) = uint16_t(st.x);
+    }
+    st.pos -= nt;
+    const uint32_t xn = rans_update(st.x, e, emit);
+    st.x = active ? xn : st.x;
+}
+
+// Symbol loads: 32 steps (t, t-1, ..., t-31) of this lane, most recent step
+// first.  volatile keeps them ahead of the steps that consume them.
+template <int DT>
+__device__ __forceinline__ void load_block(uint32_t (&v)[32], const uint8_t* cin, int32_t t, uint32_t lane,
+                                           uint64_t pol) {
     constexpr uint32_t es = Traits<DT>::kEs;
-    const uint32_t T = (n_c + 31) / 32;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const uint8_t* p = cin + es * (uint64_t(uint32_t(t - j)) * 32 + lane);
+        v[j] = es == 2 ? ld_u16_hint(p, pol) : ld_u32_hint(p, pol);
+    }
+}
+
+// Encodes steps t = T-1 .. 0.
+//   Sink::Smem   stages words below st.pos (u16 index into shared memory) and
+//                returns false, with nothing written below `limit`, if the
+//                stream would not fit;
+//   Sink::Count  only counts words (st.pos = -count) and returns false as soon
+//                as hdr_bytes + 2 * count reaches n_c (the chunk goes RAW);
+//   Sink::Global writes each word in place at gwords, st.pos counting down
+//                from the word total.
+// Full chunks run in unrolled blocks of 32 steps.  The word store of step j
+// is issued after the state update of step j + 2: its address depends on the
+// ballots of all earlier steps, and a warp issues in order, so storing at
+// once would hold back every later step on that address chain.  The staging /
+// RAW limits are tested once per block against the block's worst case (1024
+// words); a block that could cross a limit, and every step after it, runs
+// step by step with exact checks.
+template <int DT, Sink S>
+__device__ __forceinline__ void put_word(uint32_t stage_s, uint8_t* gwords, int32_t at, uint32_t w) {
+    if (S == Sink::Smem) sts_u16(stage_s + 2u * uint32_t(at), w);
+    else if (S == Sink::Global) *reinterpret_cast<uint16_t*>(gwords + 2 * uint64_t(uint32_t(at))) = uint16_t(w);
+}
+
+template <int DT, Sink S>
+__device__ bool encode_chunk(const uint8_t* __restrict__ cin, uint32_t n_c, uint32_t table_s, uint32_t stage_s,
+                             uint32_t lane, EncState& st, int32_t limit, uint8_t* gwords, uint32_t hdr_bytes,
+                             uint64_t pol) {
     const uint32_t lt = lanemask_lt();
-    uint32_t x = kRansL;
-    auto load = [&](uint32_t t) -> uint32_t {
-        const uint32_t i = 32 * t + lane;
-        if (i >= n_c) return 0;
-        return es == 2 ? ld_u16_hint(cin + 2 * uint64_t(i), pol) : ld_u32_hint(cin + 4 * uint64_t(i), pol);
-    };
-    auto step = [&](uint32_t bits, bool active) -> bool {
-        const uint4 e = *reinterpret_cast<const uint4*>(table + Traits<DT>::table_off(bits));
-        const bool emit = active && (x > e.z);
-        const uint32_t b = __ballot_sync(0xFFFFFFFFu, emit);
-        const int32_t nt = __popc(b);
+    st.x = kRansL;
+    auto step_checked = [&](uint32_t bits, bool active) -> bool {
         if (S == Sink::Smem) {
-            if (pos - nt < limit) return false;
-            if (emit) stage[pos - nt + __popc(b & lt)] = uint16_t(x);
-        } else if (S == Sink::Global) {
-            if (emit) {
-                const uint32_t wi = uint32_t(pos - nt) + __popc(b & lt);
-                *reinterpret_cast<uint16_t*>(gwords + 2 * uint64_t(wi)) = uint16_t(x);
-            }
+            const uint4 e = lds_table(table_s + Traits<DT>::table_off(bits));
+            const bool emit = active && (st.x > e.z);
+            const int32_t nt = __popc(__ballot_sync(0xFFFFFFFFu, emit));
+            if (st.pos - nt < limit) return false;
         }
-        pos -= nt;
-        if (S == Sink::Count) {
-            // pos counts down from 0: -pos words so far
-            if (hdr_bytes + 2 * uint32_t(-pos) >= n_c) return false;
-        }
-        const uint32_t xn = rans_update(x, e, emit);
-        x = active ? xn : x;
+        enc_step<DT, S>(st, bits, active, table_s, stage_s, gwords, lt);
+        if (S == Sink::Count && hdr_bytes + 2u * uint32_t(-st.pos) >= n_c) return false;
         return true;
     };
     if (n_c == kChunk) {
-        // full chunk: 2048 steps, prefetch 32 steps ahead in two register banks
-        uint32_t a[32], bnk[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) a[j] = load(kSteps - 1 - j);
-        for (int32_t t0 = kSteps - 1; t0 >= 0; t0 -= 64) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) bnk[j] = (t0 - 32 - j >= 0) ? load(t0 - 32 - j) : 0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (!step(a[j], true)) {
-                    x_out = x;
-                    return false;
+        uint32_t va[32], vb[32];
+        // delay line: words, emit flags and ballots of the two steps not yet stored
+        uint32_t w1 = 0, w2 = 0, b1 = 0, b2 = 0;
+        bool e1 = false, e2 = false;
+        auto flush_one = [&](uint32_t w, bool emit, uint32_t b) {
+            const int32_t nt = __popc(b);
+            if (emit) put_word<DT, S>(stage_s, gwords, st.pos - nt + __popc(b & lt), w);
+            st.pos -= nt;
+        };
+        bool checked = false;
+        auto run_block = [&](const uint32_t (&v)[32]) -> bool {
+            bool safe = true;
+            if (S == Sink::Smem) safe = st.pos - 32 * 32 >= limit;
+            if (S == Sink::Count) safe = hdr_bytes + 2u * uint32_t(-st.pos + 32 * 32) < n_c;
+            if (!safe && !checked) {
+                // leave the fast path: store the delayed words with exact checks
+                checked = true;
+                if (S == Sink::Smem) {
+                    if (st.pos - __popc(b2) < limit) return false;
+                    flush_one(w2, e2, b2);
+                    if (st.pos - __popc(b1) < limit) return false;
+                    flush_one(w1, e1, b1);
+                } else if (S == Sink::Global) {
+                    flush_one(w2, e2, b2);
+                    flush_one(w1, e1, b1);
                 }
-            if (t0 - 32 < 0) break;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) a[j] = (t0 - 64 - j >= 0) ? load(t0 - 64 - j) : 0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (!step(bnk[j], true)) {
-                    x_out = x;
-                    return false;
-                }
-        }
-    } else {
-        for (int32_t t = int32_t(T) - 1; t >= 0; --t) {
-            const uint32_t bits = load(uint32_t(t));
-            if (!step(bits, 32 * uint32_t(t) + lane < n_c)) {
-                x_out = x;
-                return false;
+                b1 = b2 = 0;
+                e1 = e2 = false;
             }
+            if (checked) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (!step_checked(v[j], true)) return false;
+                return true;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const uint4 e = lds_table(table_s + Traits<DT>::table_off(v[j]));
+                const bool emit = st.x > e.z;
+                const uint32_t b = __ballot_sync(0xFFFFFFFFu, emit);
+                const uint32_t w = st.x;
+                st.x = rans_update(st.x, e, emit);
+                if (S == Sink::Count) {
+                    st.pos -= __popc(b);
+                } else {
+                    flush_one(w2, e2, b2);  // step j - 2
+                    w2 = w1, e2 = e1, b2 = b1;
+                    w1 = w, e1 = emit, b1 = b;
+                }
+            }
+            if (S == Sink::Count && hdr_bytes + 2u * uint32_t(-st.pos) >= n_c) return false;
+            return true;
+        };
+        load_block<DT>(va, cin, int32_t(kSteps) - 1, lane, pol);
+        for (int32_t t0 = int32_t(kSteps) - 1;; t0 -= 64) {
+            load_block<DT>(vb, cin, t0 - 32, lane, pol);
+            if (!run_block(va)) return false;
+            const bool last = t0 == 63;
+            if (!last) load_block<DT>(va, cin, t0 - 64, lane, pol);
+            if (!run_block(vb)) return false;
+            if (last) break;
         }
+        if (!checked && S != Sink::Count) {
+            if (S == Sink::Smem && st.pos - __popc(b2) - __popc(b1) < limit) return false;
+            flush_one(w2, e2, b2);
+            flush_one(w1, e1, b1);
+        }
+        return true;
     }
-    x_out = x;
+    constexpr uint32_t es = Traits<DT>::kEs;
+    const uint32_t T = (n_c + 31) / 32;
+    for (int32_t t = int32_t(T) - 1; t >= 0; --t) {
+        const uint32_t i = 32 * uint32_t(t) + lane;
+        const bool active = i < n_c;
+        uint32_t bits = 0;
+        if (active) bits = es == 2 ? ld_u16_hint(cin + 2 * uint64_t(i), pol) : ld_u32_hint(cin + 4 * uint64_t(i), pol);
+        if (!step_checked(bits, active)) return false;
+    }
     return true;
 }
 
@@ -555,11 +635,13 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
         const uint32_t hdr = kStreamHead + 2 * nm.k_total;
 
         // 3. encode into shared staging
-        uint32_t x = kRansL;
-        int32_t pos = int32_t(kRegionA / 2);
+        const uint32_t regA_s = smem_addr(regA);
+        EncState es_smem{kRansL, int32_t(kRegionA / 2)};
         const int32_t limit = int32_t((kStageBase + hdr) / 2);
-        uint16_t* stage = reinterpret_cast<uint16_t*>(regA);
-        const bool fits = encode_chunk<DT, Sink::Smem>(cin, n_c, regA, stage, lane, x, pos, limit, nullptr, hdr, pol_stream);
+        const bool fits =
+            encode_chunk<DT, Sink::Smem>(cin, n_c, regA_s, regA_s, lane, es_smem, limit, nullptr, hdr, pol_stream);
+        const uint32_t x = es_smem.x;
+        const int32_t pos = es_smem.pos;
 
         uint32_t len = 0;
         bool raw = false;
@@ -569,10 +651,10 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
             len = hdr + 2 * w_total;
             raw = len >= n_c;
         } else {
-            int32_t cpos = 0;
-            uint32_t xc;
-            const bool coded = encode_chunk<DT, Sink::Count>(cin, n_c, regA, nullptr, lane, xc, cpos, 0, nullptr, hdr, pol_stream);
-            w_total = uint32_t(-cpos);
+            EncState es_count{kRansL, 0};
+            const bool coded =
+                encode_chunk<DT, Sink::Count>(cin, n_c, regA_s, regA_s, lane, es_count, 0, nullptr, hdr, pol_stream);
+            w_total = uint32_t(-es_count.pos);
             len = hdr + 2 * w_total;
             raw = !coded || len >= n_c;
         }
@@ -593,11 +675,10 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
                 copy_record_out(rec, len, regA + kRegionA, dst, lane);
             } else {
                 // re-encode, writing the words in place behind the stream head
-                int32_t gpos = int32_t(w_total);
-                uint32_t xg;
-                encode_chunk<DT, Sink::Global>(cin, n_c, regA, nullptr, lane, xg, gpos, 0, dst + hdr, hdr, pol_stream);
+                EncState es_glob{kRansL, int32_t(w_total)};
+                encode_chunk<DT, Sink::Global>(cin, n_c, regA_s, regA_s, lane, es_glob, 0, dst + hdr, hdr, pol_stream);
                 uint8_t* rec = regA + kStageBase;  // staging is free now: build the head there
-                write_stream_head_smem(rec, xg, nm, lane, regB);
+                write_stream_head_smem(rec, es_glob.x, nm, lane, regB);
                 __syncwarp();
                 for (uint32_t i = lane; i < hdr / 2; i += 32)
                     reinterpret_cast<uint16_t*>(dst)[i] = reinterpret_cast<const uint16_t*>(rec)[i];

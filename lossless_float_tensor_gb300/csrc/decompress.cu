@@ -172,27 +172,37 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
     }
     __syncwarp();
 
-    const uint16_t* words = reinterpret_cast<const uint16_t*>(src + kStreamHead + 2 * k_total);
+    // W == 0: any word request is an error, caught by the final pos == W
+    // test; point the (never needed) reads at the stream head, which is
+    // always inside the container.
+    const uint16_t* words =
+        W ? reinterpret_cast<const uint16_t*>(src + kStreamHead + 2 * k_total) : reinterpret_cast<const uint16_t*>(src);
+    const uint32_t wlast = W ? W - 1 : 0;
     const uint32_t lt = lanemask_lt();
+    const uint32_t slot_s = static_cast<uint32_t>(__cvta_generic_to_shared(slot_sym));
+    const uint32_t fc_s = static_cast<uint32_t>(__cvta_generic_to_shared(sym_fc));
     uint32_t pos = 0;
-    const uint32_t T = (n_c + 31) / 32;
+    // One decode step (rule R6, read side).  At most 32 words are consumed
+    // per step, so every lane first loads the word at pos + lane (pos is known
+    // from the previous step, so this load is off the state's dependency
+    // chain) and a lane that renormalises takes its word from lane
+    // popc(ballot & lanes below) with one shuffle.  Reads past the stream are
+    // clamped to its last word; they leave pos > W, which fails the check
+    // after the loop.
     auto step = [&](uint32_t t, uint32_t r, bool active) {
+        const uint32_t widx = pos + lane;
+        const uint32_t win = __ldg(words + (widx < wlast ? widx : wlast));
         const uint32_t slot = x & (kM - 1);
-        const uint32_t s = slot_sym[slot];
-        const uint32_t fc = sym_fc[s];
-        uint32_t xn = (fc & 0xFFFFu) * (x >> kProbBits) + slot - (fc >> 16);
+        uint32_t s, fc;
+        asm("ld.shared.u8 %0, [%1];" : "=r"(s) : "r"(slot_s + slot));
+        asm("ld.shared.u32 %0, [%1];" : "=r"(fc) : "r"(fc_s + 4 * s));
+        const uint32_t xn = (fc & 0xFFFFu) * (x >> kProbBits) + slot - (fc >> 16);
         const bool need = active && xn < kRansL;
         const uint32_t b = __ballot_sync(0xFFFFFFFFu, need);
-        if (need) {
-            const uint32_t wi = pos + __popc(b & lt);
-            uint32_t w = 0;
-            if (wi < W) w = words[wi];
-            else bad = true;
-            xn = (xn << 16) | w;
-        }
+        const uint32_t w = __shfl_sync(0xFFFFFFFFu, win, __popc(b & lt));
         pos += __popc(b);
         if (active) {
-            x = xn;
+            x = need ? ((xn << 16) | w) : xn;
             const uint32_t v = merge_bits<DT>(s, r);
             const uint64_t i = 32 * uint64_t(t) + lane;
             if (es == 2) reinterpret_cast<uint16_t*>(out)[i] = uint16_t(v);
@@ -202,9 +212,9 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
     auto load_rem = [&](uint32_t t) -> uint32_t {
         const uint32_t i = 32 * t + lane;
         if (i >= n_c) return 0;
-        if (DT == UZIP_BF16) return rem[i];
-        return uint32_t(rem[3 * uint64_t(i)]) | uint32_t(rem[3 * uint64_t(i) + 1]) << 8 |
-               uint32_t(rem[3 * uint64_t(i) + 2]) << 16;
+        if (DT == UZIP_BF16) return __ldg(rem + i);
+        return uint32_t(__ldg(rem + 3 * uint64_t(i))) | uint32_t(__ldg(rem + 3 * uint64_t(i) + 1)) << 8 |
+               uint32_t(__ldg(rem + 3 * uint64_t(i) + 2)) << 16;
     };
     if (n_c == kChunk) {
         uint32_t ra[16], rbk[16];
@@ -223,6 +233,7 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
             for (int j = 0; j < 16; ++j) step(t0 + 16 + j, rbk[j], true);
         }
     } else {
+        const uint32_t T = (n_c + 31) / 32;
         for (uint32_t t = 0; t < T; ++t) step(t, load_rem(t), 32 * t + lane < n_c);
     }
     const bool fail = bad || x != kRansL || pos != W;
