@@ -132,6 +132,25 @@ def gpu_id_for(dev_index: int) -> str:
         return vis.split(",")[dev_index] if vis else str(dev_index)
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The slowest rank's figure (every rank gets it).  Works on any backend:
+    the tensor lives on `device` (a CUDA device for NCCL, the CPU for gloo)."""
+    if world <= 1:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput_gbs(bytes_per_rank: int, steps: int, max_ms: float, world: int) -> float:
+    """Whole-job input GB/s: every rank compresses and decompresses its own
+    replica of the workload, so the job moves world * bytes per step, in the
+    slowest rank's time."""
+    return world * bytes_per_rank * steps / (max_ms / 1e3) / 1e9
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -187,14 +206,10 @@ def run_ours(args, rank, world, local_rank):
     tc = [e[0].elapsed_time(e[1]) for e in events]
     td = [e[1].elapsed_time(e[2]) for e in events]
     step_ms = [e[0].elapsed_time(e[2]) for e in events]
-    dev_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([dev_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dev_ms = float(t.item())
+    dev_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = dev_ms / args.steps
     in_bytes = 2 * n
-    value = world * in_bytes * args.steps / (dev_ms / 1e3) / 1e9
+    value = replica_throughput_gbs(in_bytes, args.steps, dev_ms, world)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -217,6 +232,7 @@ def run_ours(args, rank, world, local_rank):
               "peak_source": f"{peak_kind} hbm_gbs"}
     dominant = roof_c if mc >= md else roof_d
     cpu = None if args.no_cpu_baseline else cpu_baseline(bits)
+    pipe = None if args.no_pipeline else run_pipeline(args, dev)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -228,7 +244,7 @@ def run_ours(args, rank, world, local_rank):
         "ratio": total / in_bytes, "compressed_bytes": total,
         "roofline": dominant, "roofline_compress": roof_c, "roofline_decompress": roof_d,
         "clocks": clk.summary(), "e2e": e2e, "gpu_launches": 2 * args.steps,
-        "wall_s_timed_region": wall, "cpu_baseline": cpu, "kernel_source_hash": kernel_hash(),
+        "wall_s_timed_region": wall, "cpu_baseline": cpu, "pipeline": pipe, "kernel_source_hash": kernel_hash(),
     }
     return line
 
@@ -280,6 +296,70 @@ def run_e2e(args, x, bits, comp, cap, size, out, status, stream, dev, total):
             "d2h_bytes_per_step": tb + 2 * n + 8, "steps": steps, "bit_exact": ok}
 
 
+def run_pipeline(args, dev):
+    """Split-send pipeline (two streams, two ping-pong banks) on c5-shaped
+    messages: the first 1 GiB message of the Llama-3-8B-shaped parameter set
+    (bf16 ~ N(0, 0.02)) is sent `reps` times, and prefixes of it give the
+    64 KiB .. 1 GiB size sweep.  Reported: input GB/s of the pipelined modes
+    (exact-size copy kernel into mapped pinned memory; bound-size
+    cudaMemcpyAsync), of compress-then-copy on one stream (no overlap), and of a
+    plain device-to-host copy of the uncompressed bytes."""
+    import numpy as np
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+    import synth
+
+    msg = synth.c5_message(0)
+    n_max = msg.size
+    x = torch.from_numpy(msg.view(np.int16)).to(dev)
+    cap = uz.uzip_max_compressed_size(uz.UZIP_BF16, n_max)
+    banks = [torch.empty(cap, dtype=torch.uint8, device=dev) for _ in range(2)]
+    hb = [torch.empty(cap, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    h_raw = torch.empty(2 * n_max, dtype=torch.uint8).pin_memory()
+    s0, s1 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    modes = {"exact": uz.UZIP_PIPE_EXACT, "bound": uz.UZIP_PIPE_BOUND, "serial": uz.UZIP_PIPE_SERIAL}
+    sizes = [1 << 15, 1 << 17, 1 << 19, 1 << 21, 1 << 23, 1 << 25, 1 << 27, n_max]  # values (64 KiB .. 1 GiB)
+    sweep = []
+    for n in sizes:
+        reps = int(max(4, min(64, (4 << 30) // (2 * n))))
+        if n == n_max:
+            reps = args.pipeline_messages
+        hs = torch.zeros(reps, dtype=torch.int64).pin_memory()
+        row = {"message_bytes": 2 * n, "messages": reps}
+        for name, mode in modes.items():
+            for it in range(2):  # first pass warms up
+                torch.cuda.synchronize(dev)
+                t0 = time.perf_counter()
+                st = uz.uzip_pipeline_send(uz.UZIP_BF16, [x.data_ptr()] * reps, [n] * reps,
+                                           [b.data_ptr() for b in banks], cap, [h.data_ptr() for h in hb], cap,
+                                           hs.data_ptr(), mode, s0.cuda_stream, s1.cuda_stream)
+                torch.cuda.synchronize(dev)
+                dt = time.perf_counter() - t0
+                if st != 0:
+                    raise RuntimeError(f"pipeline status {st}")
+            row[name + "_gbs"] = reps * 2 * n / dt / 1e9
+        row["ratio"] = int(hs[0]) / (2 * n)
+        # plain copy of the raw bytes over the same link
+        raw = x.view(torch.uint8)[: 2 * n]
+        for it in range(2):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            with torch.cuda.stream(s1):
+                for _ in range(reps):
+                    h_raw[: 2 * n].copy_(raw, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            dt = time.perf_counter() - t0
+        row["raw_d2h_gbs"] = reps * 2 * n / dt / 1e9
+        sweep.append(row)
+    full = sweep[-1]
+    return {"workload": "c5: first 1 GiB message of the Llama-3-8B-shaped bf16 parameter set ~ N(0, 0.02), "
+                        f"sent {full['messages']} times; size sweep on its prefixes",
+            "unit": "GB/s (input bytes, host wall clock incl. sync)", "sweep": sweep,
+            "exact_gbs": full["exact_gbs"], "bound_gbs": full["bound_gbs"], "serial_gbs": full["serial_gbs"],
+            "raw_d2h_gbs": full["raw_d2h_gbs"]}
+
+
 def cpu_baseline(bits):
     """The oracle (single-threaded C) on the whole tensor, compress + decompress."""
     import oracle
@@ -329,6 +409,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-pipeline", action="store_true")
+    ap.add_argument("--pipeline-messages", type=int, default=8,
+                    help="1 GiB messages sent through the split-send pipeline")
     ap.add_argument("--elements", type=int, default=None,
                     help="use only the first N values of the workload (profiling captures)")
     args = ap.parse_args()

@@ -40,13 +40,13 @@ template <>
 struct Traits<UZIP_BF16> {
     static constexpr uint32_t kEs = 2;
     __device__ static uint32_t exp_of(uint32_t b) { return (b >> 7) & 0xFFu; }
-    __device__ static uint32_t table_off(uint32_t b) { return (b >> 3) & 0xFF0u; }  // exponent * 16
+    __device__ static uint32_t table_off(uint32_t b) { return (b >> 4) & 0x7F8u; }  // exponent * 8
 };
 template <>
 struct Traits<UZIP_FP32> {
     static constexpr uint32_t kEs = 4;
     __device__ static uint32_t exp_of(uint32_t b) { return (b >> 23) & 0xFFu; }
-    __device__ static uint32_t table_off(uint32_t b) { return (b >> 19) & 0xFF0u; }
+    __device__ static uint32_t table_off(uint32_t b) { return (b >> 20) & 0x7F8u; }
 };
 
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
@@ -109,26 +109,31 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
             st_u32_hint(d + 8, (r[2] >> 16) | (r[3] << 8), pol_stream);
         }
     };
-    // batches of U vectors per lane, two batches in flight
+    // Batches of U vectors per lane, two batches in flight, taken from the end
+    // of the chunk towards its start: the encoder re-reads the chunk backwards,
+    // so the data it needs first is the data loaded last, which keeps the
+    // longest stay in L2 as short as possible.  The ragged vectors that do not
+    // fill a batch come first, from the front.
     constexpr int U = 8;
     const uint32_t nb = nvec / (32 * U);
+    const uint32_t head = nvec - nb * 32 * U;  // vectors before the batched part
+    for (uint32_t v = lane; v < head; v += 32) process(ld_v4_hint(cin + uint64_t(v) * 16, pol_keep), v);
     uint4 qa[U], qb[U];
+    auto vec = [&](uint32_t k, int u) -> uint32_t { return head + (nb - 1 - k) * 32 * U + 32 * (U - 1 - u) + lane; };
     auto load = [&](uint4 (&q)[U], uint32_t k) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) q[u] = ld_v4_hint(cin + uint64_t(k * 32 * U + 32 * u + lane) * 16, pol_keep);
+        for (int u = 0; u < U; ++u) q[u] = ld_v4_hint(cin + uint64_t(vec(k, u)) * 16, pol_keep);
     };
     if (nb > 0) load(qa, 0);
     for (uint32_t k = 0; k < nb; k += 2) {
         if (k + 1 < nb) load(qb, k + 1);
 #pragma unroll
-        for (int u = 0; u < U; ++u) process(qa[u], k * 32 * U + 32 * u + lane);
+        for (int u = 0; u < U; ++u) process(qa[u], vec(k, u));
         if (k + 1 >= nb) break;
         if (k + 2 < nb) load(qa, k + 2);
 #pragma unroll
-        for (int u = 0; u < U; ++u) process(qb[u], (k + 1) * 32 * U + 32 * u + lane);
+        for (int u = 0; u < U; ++u) process(qb[u], vec(k + 1, u));
     }
-    uint32_t v = nb * 32 * U + lane;
-    for (; v < nvec; v += 32) process(ld_v4_hint(cin + uint64_t(v) * 16, pol_keep), v);
     // ragged tail: element by element
     for (uint32_t i = nvec * kPer + lane; i < n_c; i += 32) {
         if (DT == UZIP_BF16) {
@@ -254,7 +259,7 @@ __device__ void normalise(const uint32_t c[8], uint32_t n_c, uint32_t lane, uint
     __syncwarp();
 }
 
-// encode table entry for each present symbol: {m, add, (f << 20) - 1, (M - f) | cum << 12 | sh << 27}
+// encode table row for each present symbol: {m, add} and {(f << 20) - 1, (M - f) | cum << 12 | sh << 27}
 __device__ void build_enc_table(const Norm& nm, uint32_t lane, uint8_t* table, uint8_t* regB) {
     uint32_t lsum = 0;
 #pragma unroll
@@ -284,7 +289,8 @@ __device__ void build_enc_table(const Norm& nm, uint32_t lane, uint8_t* table, u
         e.y = dm.add;
         e.z = uint32_t((uint64_t(f) << 20) - 1);
         e.w = (kM - f) | (cums[s] << 12) | (dm.sh << 27);
-        *reinterpret_cast<uint4*>(table + 16 * s) = e;
+        *reinterpret_cast<uint2*>(table + 8 * s) = make_uint2(e.x, e.y);
+        *reinterpret_cast<uint2*>(table + 2048 + 8 * s) = make_uint2(e.z, e.w);
     }
     __syncwarp();
 }
@@ -296,9 +302,15 @@ __device__ void build_enc_table(const Norm& nm, uint32_t lane, uint8_t* table, u
 // Table loads are written as side-effect-free asm: the table does not change
 // while a chunk is encoded, so the compiler may issue them as early as it likes
 // (ahead of the staging stores of earlier steps).
+// The table is split in two arrays of 8-byte rows, {m, add} at [0, 2 KiB) and
+// {(f << 20) - 1, packed} at [2 KiB, 4 KiB): a 64-bit load is served per half
+// warp, and any 16 consecutive exponent values fall in distinct banks, so the
+// usual ~20-value exponent window costs few bank conflicts (a 16-byte row would
+// put values s and s + 8 in the same banks of every quarter warp).
 __device__ __forceinline__ uint4 lds_table(uint32_t saddr) {
     uint4 v;
-    asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
+    asm("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(saddr));
+    asm("ld.shared.v2.u32 {%0,%1}, [%2+2048];" : "=r"(v.z), "=r"(v.w) : "r"(saddr));
     return v;
 }
 __device__ __forceinline__ void sts_u16(uint32_t saddr, uint32_t v) {
@@ -448,12 +460,24 @@ __device__ bool encode_chunk(const uint8_t* __restrict__ cin, uint32_t n_c, uint
             if (S == Sink::Count && hdr_bytes + 2u * uint32_t(-st.pos) >= n_c) return false;
             return true;
         };
+        // Symbols of the block three ahead are pulled into L2 (one instruction:
+        // a 32-step block is 32 * 32 contiguous values), so a line evicted
+        // since the histogram pass is back before its register load is issued.
+        constexpr uint32_t kLines = Traits<DT>::kEs * 32 * 32 / 128;  // 128-byte lines per block
+        auto prefetch_block = [&](int32_t t_top) {
+            const int32_t t_low = t_top - 31;
+            if (t_low >= 0 && lane < kLines)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(cin + uint64_t(t_low) * 32 * Traits<DT>::kEs + 128 * lane));
+        };
         load_block<DT>(va, cin, int32_t(kSteps) - 1, lane, pol);
+        prefetch_block(int32_t(kSteps) - 65);
         for (int32_t t0 = int32_t(kSteps) - 1;; t0 -= 64) {
             load_block<DT>(vb, cin, t0 - 32, lane, pol);
+            prefetch_block(t0 - 96);
             if (!run_block(va)) return false;
             const bool last = t0 == 63;
             if (!last) load_block<DT>(va, cin, t0 - 64, lane, pol);
+            prefetch_block(t0 - 128);
             if (!run_block(vb)) return false;
             if (last) break;
         }
@@ -493,7 +517,8 @@ __device__ void write_stream_head_smem(uint8_t* dst, uint32_t x, const Norm& nm,
 
 // copy `len` bytes from shared (2-byte aligned, ending at `end`) to global
 // (16-byte aligned), zero padding the last 16-byte block.
-__device__ void copy_record_out(const uint8_t* src, uint32_t len, const uint8_t* end, uint8_t* dst, uint32_t lane) {
+__device__ void copy_record_out(const uint8_t* src, uint32_t len, const uint8_t* end, uint8_t* dst, uint32_t lane,
+                                uint64_t pol) {
     const uint32_t nb = (len + 15) / 16;
     const uintptr_t s0 = reinterpret_cast<uintptr_t>(src);
     const uint32_t mis = uint32_t(s0 & 3u);  // 0 or 2
@@ -518,7 +543,7 @@ __device__ void copy_record_out(const uint8_t* src, uint32_t len, const uint8_t*
                 else if (valid < lo + 4) o[j] &= (1u << (8 * (valid - lo))) - 1u;
             }
         }
-        *reinterpret_cast<uint4*>(dst + 16 * b) = make_uint4(o[0], o[1], o[2], o[3]);
+        st_v4_hint(dst + 16 * b, make_uint4(o[0], o[1], o[2], o[3]), pol);
     }
 }
 
@@ -672,7 +697,7 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
                 uint8_t* rec = regA + 2 * uint32_t(pos) - hdr;
                 write_stream_head_smem(rec, x, nm, lane, regB);
                 __syncwarp();
-                copy_record_out(rec, len, regA + kRegionA, dst, lane);
+                copy_record_out(rec, len, regA + kRegionA, dst, lane, pol_stream);
             } else {
                 // re-encode, writing the words in place behind the stream head
                 EncState es_glob{kRansL, int32_t(w_total)};

@@ -216,21 +216,36 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
         return uint32_t(__ldg(rem + 3 * uint64_t(i))) | uint32_t(__ldg(rem + 3 * uint64_t(i) + 1)) << 8 |
                uint32_t(__ldg(rem + 3 * uint64_t(i) + 2)) << 16;
     };
+    // The word stream is read sequentially, ~11 bytes per step: pull the lines
+    // about 40 steps ahead into L1 so a step never waits on a first touch.
+    const uint8_t* wbytes = reinterpret_cast<const uint8_t*>(words);
+    const uint32_t wbytes_last = 2 * wlast;
+    auto prefetch_words = [&]() {
+        if (lane < 2) {
+            uint32_t at = 2 * pos + 384 + 128 * lane;
+            at = at < wbytes_last ? at : wbytes_last;
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(wbytes + at));
+        }
+    };
     if (n_c == kChunk) {
-        uint32_t ra[16], rbk[16];
+        // remainder bytes prefetched PF steps ahead in two register banks
+        constexpr int PF = DT == UZIP_BF16 ? 16 : 8;
+        uint32_t ra[PF], rbk[PF];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) ra[j] = load_rem(j);
-        for (uint32_t t0 = 0; t0 < kSteps; t0 += 32) {
+        for (int j = 0; j < PF; ++j) ra[j] = load_rem(j);
+        for (uint32_t t0 = 0; t0 < kSteps; t0 += 2 * PF) {
+            prefetch_words();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) rbk[j] = load_rem(t0 + 16 + j);
+            for (int j = 0; j < PF; ++j) rbk[j] = load_rem(t0 + PF + j);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) step(t0 + j, ra[j], true);
-            if (t0 + 32 < kSteps) {
+            for (int j = 0; j < PF; ++j) step(t0 + j, ra[j], true);
+            if (DT == UZIP_BF16) prefetch_words();
+            if (t0 + 2 * PF < kSteps) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) ra[j] = load_rem(t0 + 32 + j);
+                for (int j = 0; j < PF; ++j) ra[j] = load_rem(t0 + 2 * PF + j);
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) step(t0 + 16 + j, rbk[j], true);
+            for (int j = 0; j < PF; ++j) step(t0 + PF + j, rbk[j], true);
         }
     } else {
         const uint32_t T = (n_c + 31) / 32;
