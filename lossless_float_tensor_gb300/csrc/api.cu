@@ -4,6 +4,7 @@
 #include <cuda.h>
 
 #include <cstring>
+#include <mutex>
 
 #include "uzip_internal.cuh"
 #include "../../include/uzip_debug.h"
@@ -54,6 +55,44 @@ bool device_range_ok(const void* p, uint64_t bytes) {
 }
 
 }  // namespace
+
+namespace uzip {
+namespace {
+struct ShapeEntry {
+    int dev;
+    const void* kern;
+    int threads;
+    size_t smem;
+    int sms, per_sm;
+};
+std::mutex g_shape_mutex;
+ShapeEntry g_shapes[64];
+int g_num_shapes = 0;
+}  // namespace
+
+cudaError_t launch_shape(const void* kern, int threads, size_t smem, int* sms, int* per_sm) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(g_shape_mutex);
+    for (int i = 0; i < g_num_shapes; ++i) {
+        const ShapeEntry& e = g_shapes[i];
+        if (e.dev == dev && e.kern == kern && e.threads == threads && e.smem == smem) {
+            *sms = e.sms;
+            *per_sm = e.per_sm;
+            return cudaSuccess;
+        }
+    }
+    int n_sms = 0, blocks = 0;
+    if ((err = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, threads, smem)) != cudaSuccess) return err;
+    if (blocks < 1) blocks = 1;
+    if (g_num_shapes < 64) g_shapes[g_num_shapes++] = ShapeEntry{dev, kern, threads, smem, n_sms, blocks};
+    *sms = n_sms;
+    *per_sm = blocks;
+    return cudaSuccess;
+}
+}  // namespace uzip
 
 extern "C" {
 

@@ -793,14 +793,10 @@ cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n
     a.first_ticket = C > 0 ? (first_ticket < C ? first_ticket : uint32_t(C - 1)) : 0;
     a.num_chunks = uint32_t(C);
 
-    int dev = 0;
-    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    int sms = 0;
-    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
     void (*kern)(CompressArgs) = dtype == UZIP_BF16 ? compress_kernel<UZIP_BF16> : compress_kernel<UZIP_FP32>;
-    int per_sm = 0;
-    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, kCompressSmem)) != cudaSuccess) return err;
-    if (per_sm < 1) per_sm = 1;
+    int sms = 0, per_sm = 0;
+    if ((err = launch_shape(reinterpret_cast<const void*>(kern), 32, kCompressSmem, &sms, &per_sm)) != cudaSuccess)
+        return err;
     uint64_t grid = uint64_t(per_sm) * uint64_t(sms);
     const uint64_t work = C > a.first_ticket ? C - a.first_ticket : 1;
     if (grid > work) grid = work;

@@ -311,16 +311,11 @@ cudaError_t launch_decompress(int dtype, const void* d_comp, uint64_t cap, void*
     if (d_status && (err = cudaMemsetAsync(d_status, 0, sizeof(int32_t), s)) != cudaSuccess) return err;
     DecompressArgs a{static_cast<const uint8_t*>(d_comp), cap, static_cast<uint8_t*>(d_out), n, d_status};
     const uint64_t C = num_chunks(n);  // C == 0 still launches one block to validate the header
-    int dev = 0;
-    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    int sms = 0;
-    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
     void (*kern)(DecompressArgs) = dtype == UZIP_BF16 ? decompress_kernel<UZIP_BF16> : decompress_kernel<UZIP_FP32>;
     const uint32_t smem = kDecWarps * kDecWarpSmem;
-    int per_sm = 0;
-    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecWarps * 32, smem)) != cudaSuccess)
+    int sms = 0, per_sm = 0;
+    if ((err = launch_shape(reinterpret_cast<const void*>(kern), kDecWarps * 32, smem, &sms, &per_sm)) != cudaSuccess)
         return err;
-    if (per_sm < 1) per_sm = 1;
     uint64_t grid = uint64_t(per_sm) * uint64_t(sms);
     const uint64_t need = (C + kDecWarps - 1) / kDecWarps;
     if (grid > need) grid = need;

@@ -20,10 +20,10 @@ __global__ void copy_exact_kernel(const uint8_t* __restrict__ src, uint8_t* __re
 }
 
 cudaError_t launch_copy_exact(const void* d_container, void* h_dst_mapped, cudaStream_t s) {
-    int dev = 0, sms = 0;
+    int sms = 0, per_sm = 0;
     cudaError_t err;
-    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    if ((err = launch_shape(reinterpret_cast<const void*>(copy_exact_kernel), 512, 0, &sms, &per_sm)) != cudaSuccess)
+        return err;
     copy_exact_kernel<<<dim3(uint32_t(sms) * 2), dim3(512), 0, s>>>(static_cast<const uint8_t*>(d_container),
                                                                       static_cast<uint8_t*>(h_dst_mapped));
     return cudaGetLastError();

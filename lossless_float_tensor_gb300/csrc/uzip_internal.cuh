@@ -169,6 +169,10 @@ __host__ __device__ inline DivMagic div_magic(uint32_t f) {
     return r;
 }
 
+// SM count and resident blocks per SM of `kern` on the current device, looked
+// up once per (device, kernel, block shape) and cached (api.cu).
+cudaError_t launch_shape(const void* kern, int threads, size_t smem, int* sms, int* per_sm);
+
 // launchers (compress.cu, decompress.cu, pipeline.cu)
 cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                             int32_t* d_status, uint32_t first_ticket, cudaStream_t s);
