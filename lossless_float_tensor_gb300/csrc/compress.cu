@@ -81,61 +81,85 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
     __syncwarp();
     const uint32_t lane4 = lane * 4;
     uint8_t* hl = hist + lane4;
-    constexpr uint32_t kPer = 16 / Traits<DT>::kEs;  // elements per 16-byte load
-    const uint32_t nvec = n_c / kPer;
-    // one 16-byte vector: 8 bf16 or 4 fp32 values
-    auto process = [&](const uint4 q, uint32_t vi) {
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    // A unit is 16 consecutive values (32 bytes of bf16, 64 of fp32) handled by
+    // one lane, so its remainder bytes (16 or 48) leave as full 16-byte stores.
+    constexpr uint32_t PV = DT == UZIP_BF16 ? 2 : 4;  // 16-byte vectors per unit
+    const uint32_t nunits = n_c / 16;
+    auto process = [&](const uint4 (&q)[PV], uint32_t unit) {
         if (DT == UZIP_BF16) {
-            uint32_t r[4];
+            uint32_t r[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                r[j] = ((w[j] >> 8) & 0x00800080u) | (w[j] & 0x007F007Fu);
-                atomicAdd(reinterpret_cast<uint32_t*>(hl + (w[j] & 0x7F80u)), 1u);
-                atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
+            for (int v = 0; v < 2; ++v) {
+                const uint32_t w[4] = {q[v].x, q[v].y, q[v].z, q[v].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    r[4 * v + j] = ((w[j] >> 8) & 0x00800080u) | (w[j] & 0x007F007Fu);
+                    atomicAdd(reinterpret_cast<uint32_t*>(hl + (w[j] & 0x7F80u)), 1u);
+                    atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
+                }
             }
-            st_v2_hint(rem_dst + uint64_t(vi) * 8, __byte_perm(r[0], r[1], 0x6420), __byte_perm(r[2], r[3], 0x6420),
+            st_v4_hint(rem_dst + uint64_t(unit) * 16,
+                       make_uint4(__byte_perm(r[0], r[1], 0x6420), __byte_perm(r[2], r[3], 0x6420),
+                                  __byte_perm(r[4], r[5], 0x6420), __byte_perm(r[6], r[7], 0x6420)),
                        pol_stream);
         } else {
-            uint32_t r[4];
+            uint32_t r[16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                r[j] = (w[j] & 0x7FFFFFu) | ((w[j] >> 8) & 0x800000u);
-                atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
+            for (int v = 0; v < 4; ++v) {
+                const uint32_t w[4] = {q[v].x, q[v].y, q[v].z, q[v].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    r[4 * v + j] = (w[j] & 0x7FFFFFu) | ((w[j] >> 8) & 0x800000u);
+                    atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
+                }
             }
-            uint8_t* d = rem_dst + uint64_t(vi) * 12;
-            st_u32_hint(d, r[0] | (r[1] << 24), pol_stream);
-            st_u32_hint(d + 4, (r[1] >> 8) | (r[2] << 16), pol_stream);
-            st_u32_hint(d + 8, (r[2] >> 16) | (r[3] << 8), pol_stream);
+            uint32_t o[12];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {  // 4 values -> 12 bytes
+                o[3 * g] = r[4 * g] | (r[4 * g + 1] << 24);
+                o[3 * g + 1] = (r[4 * g + 1] >> 8) | (r[4 * g + 2] << 16);
+                o[3 * g + 2] = (r[4 * g + 2] >> 16) | (r[4 * g + 3] << 8);
+            }
+            uint8_t* d = rem_dst + uint64_t(unit) * 48;
+#pragma unroll
+            for (int k = 0; k < 3; ++k) st_v4_hint(d + 16 * k, make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]), pol_stream);
         }
     };
-    // Batches of U vectors per lane, two batches in flight, taken from the end
-    // of the chunk towards its start: the encoder re-reads the chunk backwards,
-    // so the data it needs first is the data loaded last, which keeps the
-    // longest stay in L2 as short as possible.  The ragged vectors that do not
-    // fill a batch come first, from the front.
-    constexpr int U = 8;
-    const uint32_t nb = nvec / (32 * U);
-    const uint32_t head = nvec - nb * 32 * U;  // vectors before the batched part
-    for (uint32_t v = lane; v < head; v += 32) process(ld_v4_hint(cin + uint64_t(v) * 16, pol_keep), v);
-    uint4 qa[U], qb[U];
-    auto vec = [&](uint32_t k, int u) -> uint32_t { return head + (nb - 1 - k) * 32 * U + 32 * (U - 1 - u) + lane; };
-    auto load = [&](uint4 (&q)[U], uint32_t k) {
+    auto load_unit = [&](uint4 (&q)[PV], uint32_t unit) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) q[u] = ld_v4_hint(cin + uint64_t(vec(k, u)) * 16, pol_keep);
+        for (int v = 0; v < int(PV); ++v) q[v] = ld_v4_hint(cin + (uint64_t(unit) * PV + v) * 16, pol_keep);
+    };
+    // Batches of U units per lane, two batches in flight, taken from the end of
+    // the chunk towards its start: the encoder re-reads the chunk backwards, so
+    // the data it needs first is the data loaded last, which keeps the longest
+    // stay in L2 as short as possible.  Units that do not fill a batch come
+    // first, from the front.
+    constexpr int U = DT == UZIP_BF16 ? 4 : 2;
+    const uint32_t nb = nunits / (32 * U);
+    const uint32_t head = nunits - nb * 32 * U;
+    for (uint32_t u = lane; u < head; u += 32) {
+        uint4 q[PV];
+        load_unit(q, u);
+        process(q, u);
+    }
+    uint4 qa[U][PV], qb[U][PV];
+    auto unit_of = [&](uint32_t k, int u) -> uint32_t { return head + (nb - 1 - k) * 32 * U + 32 * (U - 1 - u) + lane; };
+    auto load = [&](uint4 (&q)[U][PV], uint32_t k) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) load_unit(q[u], unit_of(k, u));
     };
     if (nb > 0) load(qa, 0);
     for (uint32_t k = 0; k < nb; k += 2) {
         if (k + 1 < nb) load(qb, k + 1);
 #pragma unroll
-        for (int u = 0; u < U; ++u) process(qa[u], vec(k, u));
+        for (int u = 0; u < U; ++u) process(qa[u], unit_of(k, u));
         if (k + 1 >= nb) break;
         if (k + 2 < nb) load(qa, k + 2);
 #pragma unroll
-        for (int u = 0; u < U; ++u) process(qb[u], vec(k + 1, u));
+        for (int u = 0; u < U; ++u) process(qb[u], unit_of(k + 1, u));
     }
-    // ragged tail: element by element
-    for (uint32_t i = nvec * kPer + lane; i < n_c; i += 32) {
+    // ragged tail (n_c not a multiple of 16): element by element
+    for (uint32_t i = nunits * 16 + lane; i < n_c; i += 32) {
         if (DT == UZIP_BF16) {
             const uint32_t b = reinterpret_cast<const uint16_t*>(cin)[i];
             rem_dst[i] = uint8_t(((b >> 8) & 0x80u) | (b & 0x7Fu));

@@ -92,8 +92,11 @@ __device__ void merge_raw(const uint8_t* __restrict__ ex, const uint8_t* __restr
     }
 }
 
-// Coded chunk.  Returns false if the stream is invalid.
-template <int DT>
+// Coded chunk.  Returns false if the stream is invalid.  RING: the caller has
+// checked that the stream padded to 16 bytes lies inside the readable buffer,
+// so full chunks may stage the word stream through shared memory in 16-byte
+// lines; otherwise every word window is read from global memory.
+template <int DT, bool RING>
 __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, const uint8_t* __restrict__ rem,
                              uint8_t* __restrict__ out, uint32_t n_c, uint32_t lane, uint8_t* wsm) {
     constexpr uint32_t es = DT == UZIP_BF16 ? 2 : 4;
@@ -183,15 +186,13 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
     const uint32_t fc_s = static_cast<uint32_t>(__cvta_generic_to_shared(sym_fc));
     uint32_t pos = 0;
     // One decode step (rule R6, read side).  At most 32 words are consumed
-    // per step, so every lane first loads the word at pos + lane (pos is known
-    // from the previous step, so this load is off the state's dependency
+    // per step, so every lane first fetches the word at pos + lane (pos is
+    // known from the previous step, so the fetch is off the state's dependency
     // chain) and a lane that renormalises takes its word from lane
-    // popc(ballot & lanes below) with one shuffle.  Reads past the stream are
-    // clamped to its last word; they leave pos > W, which fails the check
-    // after the loop.
-    auto step = [&](uint32_t t, uint32_t r, bool active) {
-        const uint32_t widx = pos + lane;
-        const uint32_t win = __ldg(words + (widx < wlast ? widx : wlast));
+    // popc(ballot & lanes below) with one shuffle.  Reads past the stream
+    // return some other word and leave pos > W, which fails the check after
+    // the loop.
+    auto step = [&](uint32_t t, uint32_t r, bool active, uint32_t win) {
         const uint32_t slot = x & (kM - 1);
         uint32_t s, fc;
         asm("ld.shared.u8 %0, [%1];" : "=r"(s) : "r"(slot_s + slot));
@@ -209,6 +210,10 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
             else reinterpret_cast<uint32_t*>(out)[i] = v;
         }
     };
+    auto gwin = [&]() -> uint32_t {
+        const uint32_t widx = pos + lane;
+        return __ldg(words + (widx < wlast ? widx : wlast));
+    };
     auto load_rem = [&](uint32_t t) -> uint32_t {
         const uint32_t i = 32 * t + lane;
         if (i >= n_c) return 0;
@@ -216,19 +221,88 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
         return uint32_t(__ldg(rem + 3 * uint64_t(i))) | uint32_t(__ldg(rem + 3 * uint64_t(i) + 1)) << 8 |
                uint32_t(__ldg(rem + 3 * uint64_t(i) + 2)) << 16;
     };
-    // The word stream is read sequentially, ~11 bytes per step: pull the lines
-    // about 40 steps ahead into L1 so a step never waits on a first touch.
-    const uint8_t* wbytes = reinterpret_cast<const uint8_t*>(words);
-    const uint32_t wbytes_last = 2 * wlast;
-    auto prefetch_words = [&]() {
-        if (lane < 2) {
-            uint32_t at = 2 * pos + 384 + 128 * lane;
-            at = at < wbytes_last ? at : wbytes_last;
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(wbytes + at));
+    if (n_c == kChunk && RING) {
+        // Word stream staged in a 1 KiB ring (the present-symbol list is no
+        // longer needed): four 256-byte pieces of the stream record, piece p in
+        // slot p % 4.  Every 8 steps the ring is topped up so that it holds the
+        // worst case of the next 8 steps (8 * 32 words = 512 bytes) past pos;
+        // the piece after that is loaded into registers one period early and
+        // stored at the next top-up.
+        const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(plist));
+        const uint32_t wb0 = kStreamHead + 2 * k_total;  // byte offset of word 0 in the record
+        const uint32_t nlines = (len + 15) / 16;
+        const uint32_t npieces = (nlines + 15) / 16;
+        const bool half = lane < 16;                      // a piece is 16 lines: lanes 0..15
+        auto load_piece = [&](uint32_t piece) -> uint4 {
+            const uint32_t line = piece * 16 + (lane & 15);
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (half && line < nlines) v = __ldg(reinterpret_cast<const uint4*>(src) + line);
+            return v;
+        };
+        auto store_piece = [&](uint32_t piece, uint4 v) {
+            if (half)
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(ring_s + (piece & 3) * 256 + 16 * lane),
+                             "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                             : "memory");
+        };
+        uint32_t next_piece = 0;  // first piece not yet in the ring or in flight
+        uint4 pend = make_uint4(0, 0, 0, 0);
+        uint32_t pend_piece = 0;
+        bool has_pend = false;
+        auto top_up = [&]() {
+            if (has_pend) store_piece(pend_piece, pend);
+            has_pend = false;
+            const uint32_t cur = (wb0 + 2 * pos) >> 8;
+            uint32_t need_end = ((wb0 + 2 * (pos + 8 * 32)) >> 8) + 1;
+            need_end = need_end < npieces ? need_end : npieces;
+            while (next_piece < need_end) {  // behind: bring pieces in now
+                store_piece(next_piece, load_piece(next_piece));
+                ++next_piece;
+            }
+            __syncwarp();
+            if (next_piece < npieces && next_piece < cur + 4) {
+                pend = load_piece(next_piece);
+                pend_piece = next_piece;
+                has_pend = true;
+                ++next_piece;
+            }
+        };
+        auto rwin = [&]() -> uint32_t {
+            uint32_t v;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(*reinterpret_cast<unsigned short*>(&v)) : "r"(ring_s + ((wb0 + 2 * (pos + lane)) & 1023u)) : "memory");
+            return v & 0xFFFFu;
+        };
+        constexpr int PF = 8;
+        uint32_t ra[PF], rbk[PF];
+#pragma unroll
+        for (int j = 0; j < PF; ++j) ra[j] = load_rem(j);
+        for (uint32_t t0 = 0; t0 < kSteps; t0 += 2 * PF) {
+#pragma unroll
+            for (int j = 0; j < PF; ++j) rbk[j] = load_rem(t0 + PF + j);
+            top_up();
+#pragma unroll
+            for (int j = 0; j < PF; ++j) step(t0 + j, ra[j], true, rwin());
+            if (t0 + 2 * PF < kSteps) {
+#pragma unroll
+                for (int j = 0; j < PF; ++j) ra[j] = load_rem(t0 + 2 * PF + j);
+            }
+            top_up();
+#pragma unroll
+            for (int j = 0; j < PF; ++j) step(t0 + PF + j, rbk[j], true, rwin());
         }
-    };
-    if (n_c == kChunk) {
-        // remainder bytes prefetched PF steps ahead in two register banks
+    } else if (n_c == kChunk) {
+        // The word stream is read sequentially, ~11 bytes per step: pull the
+        // lines about 40 steps ahead into L1 so a step never waits on a first
+        // touch.
+        const uint8_t* wbytes = reinterpret_cast<const uint8_t*>(words);
+        const uint32_t wbytes_last = 2 * wlast;
+        auto prefetch_words = [&]() {
+            if (lane < 2) {
+                uint32_t at = 2 * pos + 384 + 128 * lane;
+                at = at < wbytes_last ? at : wbytes_last;
+                asm volatile("prefetch.global.L1 [%0];" ::"l"(wbytes + at));
+            }
+        };
         constexpr int PF = DT == UZIP_BF16 ? 16 : 8;
         uint32_t ra[PF], rbk[PF];
 #pragma unroll
@@ -238,25 +312,25 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
 #pragma unroll
             for (int j = 0; j < PF; ++j) rbk[j] = load_rem(t0 + PF + j);
 #pragma unroll
-            for (int j = 0; j < PF; ++j) step(t0 + j, ra[j], true);
+            for (int j = 0; j < PF; ++j) step(t0 + j, ra[j], true, gwin());
             if (DT == UZIP_BF16) prefetch_words();
             if (t0 + 2 * PF < kSteps) {
 #pragma unroll
                 for (int j = 0; j < PF; ++j) ra[j] = load_rem(t0 + 2 * PF + j);
             }
 #pragma unroll
-            for (int j = 0; j < PF; ++j) step(t0 + PF + j, rbk[j], true);
+            for (int j = 0; j < PF; ++j) step(t0 + PF + j, rbk[j], true, gwin());
         }
     } else {
         const uint32_t T = (n_c + 31) / 32;
-        for (uint32_t t = 0; t < T; ++t) step(t, load_rem(t), 32 * t + lane < n_c);
+        for (uint32_t t = 0; t < T; ++t) step(t, load_rem(t), 32 * t + lane < n_c, gwin());
     }
     const bool fail = bad || x != kRansL || pos != W;
     return !__any_sync(0xFFFFFFFFu, fail);
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kDecWarps * 32) decompress_kernel(DecompressArgs a) {
+__global__ void __launch_bounds__(kDecWarps * 32, 7) decompress_kernel(DecompressArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const uint32_t lane = threadIdx.x & 31;
     const uint32_t wid = threadIdx.x >> 5;
@@ -297,7 +371,11 @@ __global__ void __launch_bounds__(kDecWarps * 32) decompress_kernel(DecompressAr
                 if (len == n_c) merge_raw<DT>(src, rem, out, n_c, lane);
                 else good = false;
             } else {
-                good = decode_coded<DT>(src, len, rem, out, n_c, lane, wsm);
+                // the ring reads the stream in whole 16-byte lines
+                if (exp_off + off + ((uint64_t(len) + 15) & ~uint64_t(15)) <= a.cap)
+                    good = decode_coded<DT, true>(src, len, rem, out, n_c, lane, wsm);
+                else
+                    good = decode_coded<DT, false>(src, len, rem, out, n_c, lane, wsm);
             }
         }
         if (!good && lane == 0) flag_corrupt(a.status);
