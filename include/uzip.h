@@ -67,9 +67,11 @@ typedef enum {
 #define UZIP_MAX_ELEMS (1ull << 40)
 
 /* Bytes the output buffer of uzip_compress must hold for (dtype, n): the
- * largest possible container (every chunk stored RAW) plus the compressor's
- * work area of 16 + 8*C bytes behind it.  Pure host function; returns 0 for
- * an unsupported dtype or n > UZIP_MAX_ELEMS. */
+ * largest possible container (every chunk stored RAW, rounded up to 16) plus
+ * the compressor's work area behind it: 16 + 8*C bytes of counters and chunk
+ * descriptors, 256 bytes of alignment slack and min(C, 2048) slots of 64 KiB
+ * where finished chunk streams wait for their offsets.  Pure host function;
+ * returns 0 for an unsupported dtype or n > UZIP_MAX_ELEMS. */
 uint64_t uzip_max_compressed_size(uzip_dtype dtype, uint64_t n);
 
 /* Compress n elements at d_in into the container at d_out.
@@ -104,17 +106,21 @@ uzip_status uzip_compress_ex(const void* d_in, uzip_dtype dtype, uint64_t n, voi
  * must not allocate device memory of their own -- for instance a transport or
  * plugin hook that runs once per message inside someone else's memory plan,
  * where a cudaMalloc could stall the whole device and would take memory the
- * application has budgeted elsewhere.  uzip_compress needs a small work area
- * (16 + 8 * ceil(n / 65536) bytes) at the tail of its output buffer; this
- * variant keeps that work area in the library's own device memory instead: a
- * fixed array in the library, one per GPU that loads it, kept until the
- * process exits.
+ * application has budgeted elsewhere.  uzip_compress needs a work area at the
+ * tail of its output buffer (counters, chunk descriptors and a stash where
+ * finished chunks wait for their offsets); this variant keeps the counters and
+ * descriptors in the library's own device memory instead -- a fixed array in
+ * the library, one per GPU that loads it, kept until the process exits -- and
+ * places each chunk as soon as its offset is known, without a stash.
  *
  *   d_in, n, dtype   as uzip_compress; n <= UZIP_NOALLOC_MAX_ELEMS (2^30,
  *                    so the array is 131,088 bytes), else UZIP_ERR_TOO_LARGE.
  *   d_out            device, 16-byte aligned; out_capacity must be at least
- *                    the largest container, uzip_max_compressed_size(dtype, n)
- *                    - 16 - 8 * ceil(n / 65536) bytes (else UZIP_ERR_CAPACITY).
+ *                    the largest container (every chunk stored RAW):
+ *                    round16(round16(64 + 12 C) + n * rb) + (C - 1) * 65536
+ *                    + round16(n - (C - 1) * 65536) bytes for C > 0 chunks,
+ *                    64 for n = 0, with rb = 1 (bf16) or 3 (fp32) (else
+ *                    UZIP_ERR_CAPACITY).
  *   d_out_size, d_status  as uzip_compress_ex (both nullable).
  * The result is byte for byte the container uzip_compress writes.  The call
  * allocates nothing: it clears the work area with cudaMemsetAsync on s and

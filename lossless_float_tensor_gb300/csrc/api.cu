@@ -98,7 +98,7 @@ extern "C" {
 
 uint64_t uzip_max_compressed_size(uzip_dtype dtype, uint64_t n) {
     if (!valid_dtype(dtype) || n > UZIP_MAX_ELEMS) return 0;
-    return scratch_offset(dtype, n) + scratch_bytes(n);
+    return scratch_offset(dtype, n) + work_area_bytes(n);
 }
 
 uzip_status uzip_compress_ex(const void* d_in, uzip_dtype dtype, uint64_t n, void* d_out, uint64_t out_capacity,
@@ -143,7 +143,8 @@ uzip_status uzip_compress_noalloc(const void* d_in, uzip_dtype dtype, uint64_t n
         return UZIP_ERR_INVALID_ARG;
     void* scratch = nullptr;
     if (noalloc_scratch_address(&scratch) != cudaSuccess ||
-        launch_compress_with_scratch(dtype, d_in, n, d_out, d_out_size, d_status, 0, scratch, s) != cudaSuccess) {
+        launch_compress_with_scratch(dtype, d_in, n, d_out, d_out_size, d_status, 0, scratch, nullptr, s) !=
+            cudaSuccess) {
         cudaGetLastError();
         return UZIP_ERR_CUDA;
     }

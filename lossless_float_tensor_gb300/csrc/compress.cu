@@ -29,6 +29,7 @@ struct CompressArgs {
     uint64_t* desc;
     uint64_t* out_size;   // nullable
     int32_t* status_out;  // nullable
+    uint8_t* stash;       // nullable: per-warp 64 KiB slots for deferred placement
     uint32_t first_ticket;
     uint32_t num_chunks;
 };
@@ -605,28 +606,58 @@ __device__ void write_raw(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t
     }
 }
 
-// decoupled look-back: exclusive prefix of padded stream lengths before chunk c
-__device__ bool look_back(uint64_t* desc, uint32_t c, uint64_t padded, uint32_t lane, uint64_t& excl_out) {
+// Decoupled look-back.  publish_length makes chunk c's padded length visible
+// (as its inclusive prefix for chunk 0, else as an aggregate);
+// resolve_offset waits for the exclusive prefix before chunk c and publishes
+// chunk c's inclusive prefix.
+__device__ void publish_length(uint64_t* desc, uint32_t c, uint64_t padded, uint32_t lane) {
+    if (lane == 0) st_release_u64(desc + c, (c == 0 ? kDescInclusive : kDescAggregate) | padded);
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// The walk reads 128 descriptors per round trip (4 per lane, nearest first):
+// with placement deferred, the nearest published inclusive prefix can lie
+// hundreds of chunks back.  A descriptor is one 64-bit word (flag and value),
+// so a relaxed load sees both consistently.
+__device__ bool resolve_offset(uint64_t* desc, uint32_t c, uint64_t padded, uint32_t lane, uint64_t& excl_out) {
     if (c == 0) {
-        if (lane == 0) st_release_u64(desc, kDescInclusive | padded);
         excl_out = 0;
         return true;
     }
-    if (lane == 0) st_release_u64(desc + c, kDescAggregate | padded);
     uint64_t excl = 0;
     int64_t top = int64_t(c) - 1;
     uint32_t spins = 0;
     uint32_t backoff = 32;
     bool ok = true;
     while (true) {
-        const int64_t idx = top - int64_t(lane);
-        const uint64_t d = idx >= 0 ? ld_acquire_u64(desc + idx) : kDescInclusive;
-        const uint32_t flag = uint32_t(d >> 62);
-        const uint32_t incl = __ballot_sync(0xFFFFFFFFu, flag == 2);
-        const uint32_t empty = __ballot_sync(0xFFFFFFFFu, flag == 0);
-        const uint32_t first = incl ? uint32_t(__ffs(incl) - 1) : 32u;
-        const uint32_t below = first == 32 ? 0xFFFFFFFFu : ((1u << first) - 1u);
-        if (empty & below) {
+        // lane l holds descriptors top - 4l .. top - 4l - 3 (k = 0 nearest)
+        uint64_t d[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t idx = top - 4 * int64_t(lane) - k;
+            d[k] = idx >= 0 ? ld_relaxed_u64(desc + idx) : kDescInclusive;  // before chunk 0: inclusive 0
+        }
+        // first inclusive within the lane, and whether an empty one precedes it
+        uint32_t kin = 4;
+        bool empty_before = false;
+#pragma unroll
+        for (int k = 3; k >= 0; --k) {
+            if ((d[k] >> 62) == 2) kin = uint32_t(k);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (uint32_t(k) < kin && (d[k] >> 62) == 0) empty_before = true;
+        const uint32_t incl = __ballot_sync(0xFFFFFFFFu, kin < 4);
+        const uint32_t first = incl ? uint32_t(__ffs(incl) - 1) : 32u;  // lane holding the nearest inclusive
+        // any empty descriptor nearer than that inclusive?
+        const bool my_empty = lane < first ? (d[0] >> 62 == 0 || d[1] >> 62 == 0 || d[2] >> 62 == 0 || d[3] >> 62 == 0)
+                                           : (lane == first && empty_before);
+        if (__any_sync(0xFFFFFFFFu, my_empty)) {
             if (++spins > kSpinLimit) {
                 ok = false;
                 break;
@@ -635,10 +666,18 @@ __device__ bool look_back(uint64_t* desc, uint32_t c, uint64_t padded, uint32_t 
             backoff = backoff < 1024 ? backoff * 2 : 1024;
             continue;
         }
-        const uint64_t val = lane <= first ? (d & kDescValue) : 0;
+        uint64_t val = 0;
+        if (lane < first) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) val += d[k] & kDescValue;
+        } else if (lane == first) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (uint32_t(k) <= kin) val += d[k] & kDescValue;
+        }
         excl += warp_sum_u64(val);
         if (first < 32) break;
-        top -= 32;
+        top -= 128;
     }
     if (lane == 0) st_release_u64(desc + c, kDescInclusive | ((excl + padded) & kDescValue));
     excl_out = excl;
@@ -646,6 +685,10 @@ __device__ bool look_back(uint64_t* desc, uint32_t c, uint64_t padded, uint32_t 
 }
 
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 template <int DT>
 __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -661,6 +704,85 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
     const uint64_t pol_keep = policy_evict_last();
     const uint64_t pol_stream = policy_evict_first();
     const uint32_t processed = C - a.first_ticket;
+    // this warp's stash slot (one warp per block)
+    uint8_t* stash = a.stash ? a.stash + uint64_t(blockIdx.x) * kStashSlot : nullptr;
+
+    // Chunk c is placed: table entries, done counter; the warp that completes
+    // the last chunk writes the header.  Returns true for that warp.
+    auto complete = [&](uint32_t c, uint32_t len, bool raw, uint64_t excl, bool ok) -> bool {
+        if (!ok && lane == 0) atomicCAS(&a.scratch->status, 0u, uint32_t(UZIP_ERR_TIMEOUT));
+        if (ok && lane == 0) {
+            reinterpret_cast<uint64_t*>(a.out + kHeader)[c] = excl;
+            reinterpret_cast<uint32_t*>(a.out + kHeader + 8 * uint64_t(C))[c] = len | (raw ? kRawFlag : 0u);
+        }
+        __syncwarp();
+        uint32_t prev = 0;
+        if (lane == 0) {
+            __threadfence();
+            prev = atomicAdd(&a.scratch->done, 1u);
+        }
+        prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+        if (prev + 1 != processed) return false;
+        __threadfence();
+        if (lane == 0) {
+            const uint32_t st = *reinterpret_cast<volatile uint32_t*>(&a.scratch->status);
+            const uint64_t last = ld_acquire_u64(a.desc + (C - 1));
+            uint64_t total = exp_off + (last & kDescValue);
+            if (st != 0 || (last >> 62) != 2) total = 0;
+            uint8_t* h = a.out;
+            *reinterpret_cast<uint32_t*>(h) = 0x31505A55u;  // "UZP1"
+            *reinterpret_cast<uint16_t*>(h + 4) = 1;
+            h[6] = uint8_t(DT);
+            h[7] = 0;
+            *reinterpret_cast<uint64_t*>(h + 8) = n;
+            *reinterpret_cast<uint32_t*>(h + 16) = kChunk;
+            *reinterpret_cast<uint32_t*>(h + 20) = C;
+            *reinterpret_cast<uint64_t*>(h + 24) = rem_off;
+            *reinterpret_cast<uint64_t*>(h + 32) = exp_off;
+            *reinterpret_cast<uint64_t*>(h + 40) = total;
+            *reinterpret_cast<uint64_t*>(h + 48) = 0;
+            *reinterpret_cast<uint64_t*>(h + 56) = 0;
+            for (uint64_t i = kHeader + 12 * uint64_t(C); i < rem_off; ++i) h[i] = 0;
+            for (uint64_t i = rem_off + n * rb; i < exp_off; ++i) h[i] = 0;
+            if (a.out_size) *a.out_size = total;
+            if (a.status_out) *a.status_out = int32_t(st ? st : (total ? 0u : uint32_t(UZIP_ERR_TIMEOUT)));
+        }
+        return true;
+    };
+
+    // A stashed chunk (coded, staged): its 16-byte aligned, zero padded record
+    // waits in the stash slot; once its offset is known it is copied out and
+    // the slot's L2 lines are dropped without write-back.
+    bool pend = false;
+    uint32_t p_c = 0, p_len = 0;
+    auto place_pending = [&]() -> bool {
+        uint64_t excl = 0;
+        const bool ok = resolve_offset(a.desc, p_c, round16(p_len), lane, excl);
+        if (ok) {
+            // 16-byte blocks, 8 loads in flight per lane before their stores
+            const uint32_t nb = (p_len + 15) / 16;
+            uint8_t* dst = a.out + exp_off + excl;
+            const uint4* src = reinterpret_cast<const uint4*>(stash);
+            for (uint32_t b0 = 0; b0 < nb; b0 += 8 * 32) {
+                uint4 v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t b = b0 + 32 * k + lane;
+                    if (b < nb) v[k] = __ldcg(src + b);
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t b = b0 + 32 * k + lane;
+                    if (b < nb) st_v4_hint(dst + 16 * b, v[k], pol_stream);
+                }
+            }
+        }
+        __syncwarp();
+        for (uint32_t l = lane; l < (p_len + 127) / 128; l += 32) discard_l2_line(stash + 128 * l);
+        __syncwarp();
+        pend = false;
+        return complete(p_c, p_len, false, excl, ok);
+    };
 
     uint32_t* ticket = &a.scratch->ticket;
     while (C > 0) {
@@ -709,10 +831,24 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
         }
         if (raw) len = n_c;
 
-        // 4. offset by decoupled look-back
+        // 4. publish the length; place the previous stashed chunk, whose
+        //    predecessors have had a whole chunk's time to finish
+        publish_length(a.desc, c, round16(len), lane);
+        if (pend && place_pending()) return;
+        if (stash && fits && !raw) {
+            uint8_t* rec = regA + 2 * uint32_t(pos) - hdr;
+            write_stream_head_smem(rec, x, nm, lane, regB);
+            __syncwarp();
+            copy_record_out(rec, len, regA + kRegionA, stash, lane, pol_keep);
+            __syncwarp();
+            pend = true;
+            p_c = c;
+            p_len = len;
+            continue;
+        }
+        // 5. otherwise place this chunk now
         uint64_t excl = 0;
-        const bool ok = look_back(a.desc, c, round16(len), lane, excl);
-        if (!ok && lane == 0) atomicCAS(&a.scratch->status, 0u, uint32_t(UZIP_ERR_TIMEOUT));
+        const bool ok = resolve_offset(a.desc, c, round16(len), lane, excl);
         if (ok) {
             uint8_t* dst = a.out + exp_off + excl;
             if (raw) {
@@ -733,46 +869,11 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
                     reinterpret_cast<uint16_t*>(dst)[i] = reinterpret_cast<const uint16_t*>(rec)[i];
                 for (uint32_t i = len + lane; i < round16(len); i += 32) dst[i] = 0;
             }
-            if (lane == 0) {
-                reinterpret_cast<uint64_t*>(a.out + kHeader)[c] = excl;
-                reinterpret_cast<uint32_t*>(a.out + kHeader + 8 * uint64_t(C))[c] = len | (raw ? kRawFlag : 0u);
-            }
         }
         __syncwarp();
-        // 5. the last chunk to finish writes the header
-        uint32_t prev = 0;
-        if (lane == 0) {
-            __threadfence();
-            prev = atomicAdd(&a.scratch->done, 1u);
-        }
-        prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
-        if (prev + 1 != processed) continue;
-        __threadfence();
-        if (lane == 0) {
-            const uint32_t st = *reinterpret_cast<volatile uint32_t*>(&a.scratch->status);
-            const uint64_t last = ld_acquire_u64(a.desc + (C - 1));
-            uint64_t total = exp_off + (last & kDescValue);
-            if (st != 0 || (last >> 62) != 2) total = 0;
-            uint8_t* h = a.out;
-            *reinterpret_cast<uint32_t*>(h) = 0x31505A55u;  // "UZP1"
-            *reinterpret_cast<uint16_t*>(h + 4) = 1;
-            h[6] = uint8_t(DT);
-            h[7] = 0;
-            *reinterpret_cast<uint64_t*>(h + 8) = n;
-            *reinterpret_cast<uint32_t*>(h + 16) = kChunk;
-            *reinterpret_cast<uint32_t*>(h + 20) = C;
-            *reinterpret_cast<uint64_t*>(h + 24) = rem_off;
-            *reinterpret_cast<uint64_t*>(h + 32) = exp_off;
-            *reinterpret_cast<uint64_t*>(h + 40) = total;
-            *reinterpret_cast<uint64_t*>(h + 48) = 0;
-            *reinterpret_cast<uint64_t*>(h + 56) = 0;
-            for (uint64_t i = kHeader + 12 * uint64_t(C); i < rem_off; ++i) h[i] = 0;
-            for (uint64_t i = rem_off + n * rb; i < exp_off; ++i) h[i] = 0;
-            if (a.out_size) *a.out_size = total;
-            if (a.status_out) *a.status_out = int32_t(st ? st : (total ? 0u : uint32_t(UZIP_ERR_TIMEOUT)));
-        }
-        break;
+        if (complete(c, len, raw, excl, ok)) return;
     }
+    if (pend && place_pending()) return;
     // empty tensor: header only, written by the single launched warp
     if (C == 0 && blockIdx.x == 0 && lane == 0) {
         uint8_t* h = a.out;
@@ -800,7 +901,8 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
 // look-back descriptors: scratch_bytes(n) bytes) at `scratch`, which is
 // zeroed on `s` first.
 cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
-                                         int32_t* d_status, uint32_t first_ticket, void* scratch_area, cudaStream_t s) {
+                                         int32_t* d_status, uint32_t first_ticket, void* scratch_area, void* stash,
+                                         cudaStream_t s) {
     const uint64_t C = num_chunks(n);
     uint8_t* out = static_cast<uint8_t*>(d_out);
     Scratch* scratch = static_cast<Scratch*>(scratch_area);
@@ -816,6 +918,7 @@ cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n
     a.status_out = d_status;
     a.first_ticket = C > 0 ? (first_ticket < C ? first_ticket : uint32_t(C - 1)) : 0;
     a.num_chunks = uint32_t(C);
+    a.stash = static_cast<uint8_t*>(stash);
 
     void (*kern)(CompressArgs) = dtype == UZIP_BF16 ? compress_kernel<UZIP_BF16> : compress_kernel<UZIP_FP32>;
     int sms = 0, per_sm = 0;
@@ -824,18 +927,20 @@ cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n
     uint64_t grid = uint64_t(per_sm) * uint64_t(sms);
     const uint64_t work = C > a.first_ticket ? C - a.first_ticket : 1;
     if (grid > work) grid = work;
+    if (stash && grid > stash_slots(n)) grid = stash_slots(n);  // one stash slot per warp
     if (grid < 1) grid = 1;
     kern<<<dim3(uint32_t(grid)), dim3(32), kCompressSmem, s>>>(a);
     return cudaGetLastError();
 }
 
-// The regular path: the work area sits in the caller's output buffer, behind
-// the largest possible container.
+// The regular path: the work area (counters, descriptors, stash) sits in the
+// caller's output buffer, behind the largest possible container.
 cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                             int32_t* d_status, uint32_t first_ticket, cudaStream_t s) {
-    uint8_t* out = static_cast<uint8_t*>(d_out);
-    return launch_compress_with_scratch(dtype, d_in, n, d_out, d_out_size, d_status, first_ticket,
-                                        out + scratch_offset(dtype, n), s);
+    uint8_t* work = static_cast<uint8_t*>(d_out) + scratch_offset(dtype, n);
+    const uintptr_t st = (reinterpret_cast<uintptr_t>(work) + scratch_bytes(n) + 255) & ~uintptr_t(255);
+    return launch_compress_with_scratch(dtype, d_in, n, d_out, d_out_size, d_status, first_ticket, work,
+                                        reinterpret_cast<void*>(st), s);
 }
 
 // ---------------------------------------------------------------------------

@@ -47,7 +47,22 @@ struct Scratch {
 };
 constexpr uint64_t kScratchHead = 16;
 __host__ __device__ inline uint64_t scratch_offset(int dtype, uint64_t n) { return round16(container_bound(dtype, n)); }
+// status, ticket, done counter and look-back descriptors (zeroed before each launch)
 __host__ __device__ inline uint64_t scratch_bytes(uint64_t n) { return kScratchHead + 8 * num_chunks(n); }
+// Stash: one 64 KiB slot per resident warp (at most kStashSlots warps), where a
+// chunk's finished stream waits for its offset while the warp moves on.  It is
+// never read before it is written.
+constexpr uint64_t kStashSlots = 2048;
+constexpr uint64_t kStashSlot = 65536;
+__host__ __device__ inline uint64_t stash_slots(uint64_t n) {
+    const uint64_t c = num_chunks(n);
+    return c < kStashSlots ? c : kStashSlots;
+}
+// The stash starts at the first 256-byte aligned address (absolute) after the
+// descriptors; 256 bytes of slack cover the alignment.
+__host__ __device__ inline uint64_t work_area_bytes(uint64_t n) {
+    return scratch_bytes(n) + 256 + stash_slots(n) * kStashSlot;
+}
 
 // look-back descriptor: flag in bits 62..63, byte count in bits 0..61
 constexpr uint64_t kDescAggregate = 1ull << 62;
@@ -177,7 +192,8 @@ cudaError_t launch_shape(const void* kern, int threads, size_t smem, int* sms, i
 cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                             int32_t* d_status, uint32_t first_ticket, cudaStream_t s);
 cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
-                                         int32_t* d_status, uint32_t first_ticket, void* scratch_area, cudaStream_t s);
+                                         int32_t* d_status, uint32_t first_ticket, void* scratch_area, void* stash,
+                                         cudaStream_t s);
 
 // allocation-free compression: largest tensor and device count served by the
 // library's own work area
