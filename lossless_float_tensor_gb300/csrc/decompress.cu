@@ -272,11 +272,28 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
             asm volatile("ld.shared.u16 %0, [%1];" : "=h"(*reinterpret_cast<unsigned short*>(&v)) : "r"(ring_s + ((wb0 + 2 * (pos + lane)) & 1023u)) : "memory");
             return v & 0xFFFFu;
         };
+        // Both streams are cold in L2 when decompression starts: pull the
+        // remainder bytes of the steps 64 ahead and the stream bytes ~1 KiB
+        // past the read position into L2 (one instruction each per 16 steps).
+        constexpr uint32_t rb = DT == UZIP_BF16 ? 1 : 3;
+        constexpr uint32_t kRemLines = 16 * 32 * rb / 128;
+        auto prefetch_l2 = [&](uint32_t t_ahead) {
+            if (lane < kRemLines && t_ahead + 16 <= kSteps)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(rem + uint64_t(t_ahead) * 32 * rb + 128 * lane));
+            if (lane >= 30) {
+                const uint32_t at = wb0 + 2 * pos + 1024 + 128 * (lane - 30);
+                if (at < nlines * 16) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + at));
+            }
+        };
         constexpr int PF = 8;
         uint32_t ra[PF], rbk[PF];
 #pragma unroll
         for (int j = 0; j < PF; ++j) ra[j] = load_rem(j);
+        prefetch_l2(16);
+        prefetch_l2(32);
+        prefetch_l2(48);
         for (uint32_t t0 = 0; t0 < kSteps; t0 += 2 * PF) {
+            prefetch_l2(t0 + 64);
 #pragma unroll
             for (int j = 0; j < PF; ++j) rbk[j] = load_rem(t0 + PF + j);
             top_up();
