@@ -69,8 +69,9 @@ typedef enum {
 /* Bytes the output buffer of uzip_compress must hold for (dtype, n): the
  * largest possible container (every chunk stored RAW, rounded up to 16) plus
  * the compressor's work area behind it: 16 + 8*C bytes of counters and chunk
- * descriptors, 256 bytes of alignment slack and min(C, 2048) slots of 64 KiB
- * where finished chunk streams wait for their offsets.  Pure host function;
+ * descriptors, 256 bytes of alignment slack and min(C, 1536) pairs of 68 KiB
+ * slots (each compressing warp uses two, in turn, for a chunk's exponent bytes
+ * and then for its finished stream while it waits for its offset).  Pure host function;
  * returns 0 for an unsupported dtype or n > UZIP_MAX_ELEMS. */
 uint64_t uzip_max_compressed_size(uzip_dtype dtype, uint64_t n);
 
@@ -107,11 +108,12 @@ uzip_status uzip_compress_ex(const void* d_in, uzip_dtype dtype, uint64_t n, voi
  * plugin hook that runs once per message inside someone else's memory plan,
  * where a cudaMalloc could stall the whole device and would take memory the
  * application has budgeted elsewhere.  uzip_compress needs a work area at the
- * tail of its output buffer (counters, chunk descriptors and a stash where
- * finished chunks wait for their offsets); this variant keeps the counters and
- * descriptors in the library's own device memory instead -- a fixed array in
- * the library, one per GPU that loads it, kept until the process exits -- and
- * places each chunk as soon as its offset is known, without a stash.
+ * tail of its output buffer (counters, chunk descriptors and per-warp slots
+ * for exponent bytes and finished streams); this variant keeps the counters
+ * and descriptors in the library's own device memory instead -- a fixed array
+ * in the library, one per GPU that loads it, kept until the process exits --
+ * and does without the slots: each chunk is encoded twice from the input
+ * (counting, then writing in place), so it is slower than uzip_compress.
  *
  *   d_in, n, dtype   as uzip_compress; n <= UZIP_NOALLOC_MAX_ELEMS (2^30,
  *                    so the array is 131,088 bytes), else UZIP_ERR_TOO_LARGE.

@@ -3,24 +3,28 @@
 // and the output placement run in one pass without cross-block
 // synchronisation).  Per chunk the warp
 //   1. streams the chunk once, writes its sign|fraction bytes straight to the
-//      remainder plane and counts exponent bytes in a lane-private histogram;
+//      remainder plane, writes its exponent bytes to the warp's slot in the
+//      work area and counts them in a lane-private histogram;
 //   2. normalises the histogram to 4096 (largest remainder) and builds the
 //      encode table;
-//   3. runs the 32-state interleaved rANS encoder backwards over the chunk,
-//      re-reading the exponents from L2, staging the words in shared memory;
-//   4. learns its output offset by a decoupled look-back over the chunks
+//   3. runs the 32-state interleaved rANS encoder backwards over the exponent
+//      bytes of the slot, writing the words backwards from the slot's end;
+//   4. publishes its stream length for the decoupled look-back over the chunks
 //      before it (Merrill and Garland, "Single-pass parallel prefix scan with
-//      decoupled look-back", 2016) and copies the staged stream out with
-//      16-byte stores.
-// A chunk whose stream does not fit the staging area is re-encoded twice
-// (count, then write in place); a chunk that coding does not shrink is stored
-// RAW (NCCLZ Sec. IV-C).
+//      decoupled look-back", 2016) and, after its next chunk, copies the
+//      stream to its offset with 16-byte stores.
+// Each warp owns two 64 KiB slots used in turn, so a finished stream can wait
+// for its offset while the next chunk is counted.  A chunk whose words would
+// reach exponent bytes not yet read (over 4 bits per value), a partial last
+// chunk, and every chunk when no slots are given (the allocation-free entry
+// point) are encoded twice from the input instead: once counting, once
+// writing in place.  A chunk that coding does not shrink is stored RAW
+// (NCCLZ Sec. IV-C).
 #include <mutex>
 
 #include "uzip_internal.cuh"
 
 namespace uzip {
-
 struct CompressArgs {
     const uint8_t* in;
     uint64_t n;
@@ -29,7 +33,7 @@ struct CompressArgs {
     uint64_t* desc;
     uint64_t* out_size;   // nullable
     int32_t* status_out;  // nullable
-    uint8_t* stash;       // nullable: per-warp 64 KiB slots for deferred placement
+    uint8_t* stash;       // nullable: two slots of kSlotBytes per warp (exponent bytes, then the stream)
     uint32_t first_ticket;
     uint32_t num_chunks;
 };
@@ -67,37 +71,47 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t lane, ui
 }
 
 // ---------------------------------------------------------------------------
-// phase 1: plane split + lane-private histogram
-// hist layout: u32 [256 exponent values][32 lanes]; lane l only touches column
-// l, so the 32 increments of one instruction hit 32 distinct banks.
+// phase 1: plane split + exponent bytes + lane-private histogram
+// hist layout: u32 [256 exponent values][16 columns]; lane l counts in column
+// l mod 16 (16 KiB in all).  Lanes l and l + 16 share a column, so the atomic
+// increments stay exact; within one instruction they meet only when both see
+// exponents of equal parity.
 template <int DT>
 __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* __restrict__ rem_dst,
-                                uint8_t* hist, uint32_t lane, uint64_t pol_keep, uint64_t pol_stream) {
-    // zero the histogram: 32 KiB, 64 x 16 bytes per lane
+                                uint8_t* __restrict__ ex_dst, uint8_t* hist, uint32_t lane, uint64_t pol_keep,
+                                uint64_t pol_stream) {
     {
-        uint4 z = make_uint4(0, 0, 0, 0);
+        const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll 8
         for (uint32_t i = lane; i < kRegionA / 16; i += 32) reinterpret_cast<uint4*>(hist)[i] = z;
     }
     __syncwarp();
-    const uint32_t lane4 = lane * 4;
-    uint8_t* hl = hist + lane4;
+    uint8_t* hl = hist + 4 * (lane & 15);
+    auto count = [&](uint32_t e64) {  // e64 = exponent * 64
+        atomicAdd(reinterpret_cast<uint32_t*>(hl + e64), 1u);
+    };
     // A unit is 16 consecutive values (32 bytes of bf16, 64 of fp32) handled by
-    // one lane, so its remainder bytes (16 or 48) leave as full 16-byte stores.
+    // one lane: its remainder bytes (16 or 48) and exponent bytes (16) leave as
+    // full 16-byte stores.
     constexpr uint32_t PV = DT == UZIP_BF16 ? 2 : 4;  // 16-byte vectors per unit
     const uint32_t nunits = n_c / 16;
     auto process = [&](const uint4 (&q)[PV], uint32_t unit) {
+        uint32_t ex[4];
         if (DT == UZIP_BF16) {
             uint32_t r[8];
 #pragma unroll
             for (int v = 0; v < 2; ++v) {
                 const uint32_t w[4] = {q[v].x, q[v].y, q[v].z, q[v].w};
+                uint32_t eb[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     r[4 * v + j] = ((w[j] >> 8) & 0x00800080u) | (w[j] & 0x007F007Fu);
-                    atomicAdd(reinterpret_cast<uint32_t*>(hl + (w[j] & 0x7F80u)), 1u);
-                    atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
+                    eb[j] = (w[j] >> 7) & 0x00FF00FFu;  // exponents of both values, bytes 0 and 2
+                    count((eb[j] << 6) & 0x3FC0u);
+                    count((eb[j] >> 10) & 0x3FC0u);
                 }
+                ex[2 * v] = __byte_perm(eb[0], eb[1], 0x6420);
+                ex[2 * v + 1] = __byte_perm(eb[2], eb[3], 0x6420);
             }
             st_v4_hint(rem_dst + uint64_t(unit) * 16,
                        make_uint4(__byte_perm(r[0], r[1], 0x6420), __byte_perm(r[2], r[3], 0x6420),
@@ -111,8 +125,10 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     r[4 * v + j] = (w[j] & 0x7FFFFFu) | ((w[j] >> 8) & 0x800000u);
-                    atomicAdd(reinterpret_cast<uint32_t*>(hl + ((w[j] >> 16) & 0x7F80u)), 1u);
+                    count((w[j] >> 17) & 0x3FC0u);
                 }
+                ex[v] = ((w[0] >> 23) & 0xFFu) | ((w[1] >> 15) & 0xFF00u) | ((w[2] >> 7) & 0xFF0000u) |
+                        ((w[3] << 1) & 0xFF000000u);
             }
             uint32_t o[12];
 #pragma unroll
@@ -123,18 +139,16 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
             }
             uint8_t* d = rem_dst + uint64_t(unit) * 48;
 #pragma unroll
-            for (int k = 0; k < 3; ++k) st_v4_hint(d + 16 * k, make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]), pol_stream);
+            for (int k = 0; k < 3; ++k)
+                st_v4_hint(d + 16 * k, make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]), pol_stream);
         }
+        if (ex_dst) *reinterpret_cast<uint4*>(ex_dst + 16 * uint64_t(unit)) = make_uint4(ex[0], ex[1], ex[2], ex[3]);
     };
     auto load_unit = [&](uint4 (&q)[PV], uint32_t unit) {
 #pragma unroll
-        for (int v = 0; v < int(PV); ++v) q[v] = ld_v4_hint(cin + (uint64_t(unit) * PV + v) * 16, pol_keep);
+        for (int v = 0; v < int(PV); ++v) q[v] = ld_v4_hint(cin + (uint64_t(unit) * PV + v) * 16, pol_stream);
     };
-    // Batches of U units per lane, two batches in flight, taken from the end of
-    // the chunk towards its start: the encoder re-reads the chunk backwards, so
-    // the data it needs first is the data loaded last, which keeps the longest
-    // stay in L2 as short as possible.  Units that do not fill a batch come
-    // first, from the front.
+    // Batches of U units per lane, two batches in flight.
     constexpr int U = DT == UZIP_BF16 ? 4 : 2;
     const uint32_t nb = nunits / (32 * U);
     const uint32_t head = nunits - nb * 32 * U;
@@ -144,7 +158,7 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
         process(q, u);
     }
     uint4 qa[U][PV], qb[U][PV];
-    auto unit_of = [&](uint32_t k, int u) -> uint32_t { return head + (nb - 1 - k) * 32 * U + 32 * (U - 1 - u) + lane; };
+    auto unit_of = [&](uint32_t k, int u) -> uint32_t { return head + k * 32 * U + 32 * u + lane; };
     auto load = [&](uint4 (&q)[U][PV], uint32_t k) {
 #pragma unroll
         for (int u = 0; u < U; ++u) load_unit(q[u], unit_of(k, u));
@@ -161,33 +175,35 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
     }
     // ragged tail (n_c not a multiple of 16): element by element
     for (uint32_t i = nunits * 16 + lane; i < n_c; i += 32) {
+        uint32_t e;
         if (DT == UZIP_BF16) {
             const uint32_t b = reinterpret_cast<const uint16_t*>(cin)[i];
             rem_dst[i] = uint8_t(((b >> 8) & 0x80u) | (b & 0x7Fu));
-            atomicAdd(reinterpret_cast<uint32_t*>(hl + (b & 0x7F80u)), 1u);
+            e = (b >> 7) & 0xFFu;
         } else {
             const uint32_t b = reinterpret_cast<const uint32_t*>(cin)[i];
             const uint32_t r = (b & 0x7FFFFFu) | ((b >> 8) & 0x800000u);
             rem_dst[3 * uint64_t(i)] = uint8_t(r);
             rem_dst[3 * uint64_t(i) + 1] = uint8_t(r >> 8);
             rem_dst[3 * uint64_t(i) + 2] = uint8_t(r >> 16);
-            atomicAdd(reinterpret_cast<uint32_t*>(hl + ((b >> 16) & 0x7F80u)), 1u);
+            e = (b >> 23) & 0xFFu;
         }
+        count(e << 6);
+        if (ex_dst) ex_dst[i] = uint8_t(e);
     }
     __syncwarp();
 }
 
-// counts of symbols 8*lane .. 8*lane+7 from the lane-private histogram; the
-// column order is staggered by lane so each quarter-warp reads 8 distinct
-// 16-byte groups (no bank conflicts).
+// counts of symbols 8*lane .. 8*lane+7: the 16 columns of each row, read as
+// 4 x 16 bytes in a lane-staggered order
 __device__ void reduce_hist(const uint8_t* hist, uint32_t lane, uint32_t c[8]) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const uint8_t* row = hist + (8 * lane + k) * 128;
+        const uint8_t* row = hist + (8 * lane + k) * 64;
         uint32_t s = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint4 q = *reinterpret_cast<const uint4*>(row + ((j + lane) & 7) * 16);
+        for (int j = 0; j < 4; ++j) {
+            const uint4 q = *reinterpret_cast<const uint4*>(row + ((j + lane) & 3) * 16);
             s += q.x + q.y + q.z + q.w;
         }
         c[k] = s;
@@ -355,26 +371,23 @@ __device__ __forceinline__ uint32_t rans_update(uint32_t x, const uint4 e, bool 
     return q * mmf + (xr + cum);
 }
 
-enum class Sink { Smem, Count, Global };
+enum class Sink { Count, Global };
 
 struct EncState {
     uint32_t x;     // this lane's rANS state
-    int32_t pos;    // Smem: u16 index below which the next words go; Count: -words; Global: words left
+    int32_t pos;    // Count: -words so far; Global / slot: u16 index below which the next words go
 };
 
-// One encode step for one lane.  No branches: the word store is predicated.
+// One encode step for one lane (symbol from an input value).
 template <int DT, Sink S>
-__device__ __forceinline__ void enc_step(EncState& st, uint32_t bits, bool active, uint32_t table_s, uint32_t stage_s,
-                                         uint8_t* gwords, uint32_t lt) {
+__device__ __forceinline__ void enc_step(EncState& st, uint32_t bits, bool active, uint32_t table_s, uint8_t* gwords,
+                                         uint32_t lt) {
     const uint4 e = lds_table(table_s + Traits<DT>::table_off(bits));
     const bool emit = active && (st.x > e.z);
     const uint32_t b = __ballot_sync(0xFFFFFFFFu, emit);
     const int32_t nt = __popc(b);
-    if (S == Sink::Smem) {
-        if (emit) sts_u16(stage_s + 2u * uint32_t(st.pos - nt + __popc(b & lt)), st.x);
-    } else if (S == Sink::Global) {
-        if (emit) *reinterpret_cast<uint16_t*>(gwords + 2 * uint64_t(uint32_t(st.pos - nt) + __popc(b & lt))) = uint16_t(st.x);
-    }
+    if (S == Sink::Global && emit)
+        *reinterpret_cast<uint16_t*>(gwords + 2 * uint64_t(uint32_t(st.pos - nt) + __popc(b & lt))) = uint16_t(st.x);
     st.pos -= nt;
     const uint32_t xn = rans_update(st.x, e, emit);
     st.x = active ? xn : st.x;
@@ -393,144 +406,130 @@ __device__ __forceinline__ void load_block(uint32_t (&v)[32], const uint8_t* cin
     }
 }
 
-// Encodes steps t = T-1 .. 0.
-//   Sink::Smem   stages words below st.pos (u16 index into shared memory) and
-//                returns false, with nothing written below `limit`, if the
-//                stream would not fit;
+// Encoder over the input values, used when the fast path cannot run.
 //   Sink::Count  only counts words (st.pos = -count) and returns false as soon
 //                as hdr_bytes + 2 * count reaches n_c (the chunk goes RAW);
 //   Sink::Global writes each word in place at gwords, st.pos counting down
 //                from the word total.
-// Full chunks run in unrolled blocks of 32 steps.  The word store of step j
-// is issued after the state update of step j + 2: its address depends on the
-// ballots of all earlier steps, and a warp issues in order, so storing at
-// once would hold back every later step on that address chain.  The staging /
-// RAW limits are tested once per block against the block's worst case (1024
-// words); a block that could cross a limit, and every step after it, runs
-// step by step with exact checks.
 template <int DT, Sink S>
-__device__ __forceinline__ void put_word(uint32_t stage_s, uint8_t* gwords, int32_t at, uint32_t w) {
-    if (S == Sink::Smem) sts_u16(stage_s + 2u * uint32_t(at), w);
-    else if (S == Sink::Global) *reinterpret_cast<uint16_t*>(gwords + 2 * uint64_t(uint32_t(at))) = uint16_t(w);
-}
-
-template <int DT, Sink S>
-__device__ bool encode_chunk(const uint8_t* __restrict__ cin, uint32_t n_c, uint32_t table_s, uint32_t stage_s,
-                             uint32_t lane, EncState& st, int32_t limit, uint8_t* gwords, uint32_t hdr_bytes,
-                             uint64_t pol) {
+__device__ bool encode_chunk(const uint8_t* __restrict__ cin, uint32_t n_c, uint32_t table_s, uint32_t lane,
+                             EncState& st, uint8_t* gwords, uint32_t hdr_bytes, uint64_t pol) {
     const uint32_t lt = lanemask_lt();
+    constexpr uint32_t es = Traits<DT>::kEs;
     st.x = kRansL;
-    auto step_checked = [&](uint32_t bits, bool active) -> bool {
-        if (S == Sink::Smem) {
-            const uint4 e = lds_table(table_s + Traits<DT>::table_off(bits));
-            const bool emit = active && (st.x > e.z);
-            const int32_t nt = __popc(__ballot_sync(0xFFFFFFFFu, emit));
-            if (st.pos - nt < limit) return false;
-        }
-        enc_step<DT, S>(st, bits, active, table_s, stage_s, gwords, lt);
-        if (S == Sink::Count && hdr_bytes + 2u * uint32_t(-st.pos) >= n_c) return false;
-        return true;
-    };
     if (n_c == kChunk) {
         uint32_t va[32], vb[32];
-        // delay line: words, emit flags and ballots of the two steps not yet stored
-        uint32_t w1 = 0, w2 = 0, b1 = 0, b2 = 0;
-        bool e1 = false, e2 = false;
-        auto flush_one = [&](uint32_t w, bool emit, uint32_t b) {
-            const int32_t nt = __popc(b);
-            if (emit) put_word<DT, S>(stage_s, gwords, st.pos - nt + __popc(b & lt), w);
-            st.pos -= nt;
-        };
-        bool checked = false;
         auto run_block = [&](const uint32_t (&v)[32]) -> bool {
-            bool safe = true;
-            if (S == Sink::Smem) safe = st.pos - 32 * 32 >= limit;
-            if (S == Sink::Count) safe = hdr_bytes + 2u * uint32_t(-st.pos + 32 * 32) < n_c;
-            if (!safe && !checked) {
-                // leave the fast path: store the delayed words with exact checks
-                checked = true;
-                if (S == Sink::Smem) {
-                    if (st.pos - __popc(b2) < limit) return false;
-                    flush_one(w2, e2, b2);
-                    if (st.pos - __popc(b1) < limit) return false;
-                    flush_one(w1, e1, b1);
-                } else if (S == Sink::Global) {
-                    flush_one(w2, e2, b2);
-                    flush_one(w1, e1, b1);
-                }
-                b1 = b2 = 0;
-                e1 = e2 = false;
-            }
-            if (checked) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (!step_checked(v[j], true)) return false;
-                return true;
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const uint4 e = lds_table(table_s + Traits<DT>::table_off(v[j]));
-                const bool emit = st.x > e.z;
-                const uint32_t b = __ballot_sync(0xFFFFFFFFu, emit);
-                const uint32_t w = st.x;
-                st.x = rans_update(st.x, e, emit);
-                if (S == Sink::Count) {
-                    st.pos -= __popc(b);
-                } else {
-                    flush_one(w2, e2, b2);  // step j - 2
-                    w2 = w1, e2 = e1, b2 = b1;
-                    w1 = w, e1 = emit, b1 = b;
-                }
-            }
-            if (S == Sink::Count && hdr_bytes + 2u * uint32_t(-st.pos) >= n_c) return false;
-            return true;
-        };
-        // Symbols of the block three ahead are pulled into L2 (one instruction:
-        // a 32-step block is 32 * 32 contiguous values), so a line evicted
-        // since the histogram pass is back before its register load is issued.
-        constexpr uint32_t kLines = Traits<DT>::kEs * 32 * 32 / 128;  // 128-byte lines per block
-        auto prefetch_block = [&](int32_t t_top) {
-            const int32_t t_low = t_top - 31;
-            if (t_low >= 0 && lane < kLines)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(cin + uint64_t(t_low) * 32 * Traits<DT>::kEs + 128 * lane));
+            for (int j = 0; j < 32; ++j) enc_step<DT, S>(st, v[j], true, table_s, gwords, lt);
+            return !(S == Sink::Count && hdr_bytes + 2u * uint32_t(-st.pos) >= n_c);
         };
         load_block<DT>(va, cin, int32_t(kSteps) - 1, lane, pol);
-        prefetch_block(int32_t(kSteps) - 65);
         for (int32_t t0 = int32_t(kSteps) - 1;; t0 -= 64) {
             load_block<DT>(vb, cin, t0 - 32, lane, pol);
-            prefetch_block(t0 - 96);
             if (!run_block(va)) return false;
             const bool last = t0 == 63;
             if (!last) load_block<DT>(va, cin, t0 - 64, lane, pol);
-            prefetch_block(t0 - 128);
             if (!run_block(vb)) return false;
             if (last) break;
         }
-        if (!checked && S != Sink::Count) {
-            if (S == Sink::Smem && st.pos - __popc(b2) - __popc(b1) < limit) return false;
-            flush_one(w2, e2, b2);
-            flush_one(w1, e1, b1);
-        }
         return true;
     }
-    constexpr uint32_t es = Traits<DT>::kEs;
     const uint32_t T = (n_c + 31) / 32;
     for (int32_t t = int32_t(T) - 1; t >= 0; --t) {
         const uint32_t i = 32 * uint32_t(t) + lane;
         const bool active = i < n_c;
         uint32_t bits = 0;
         if (active) bits = es == 2 ? ld_u16_hint(cin + 2 * uint64_t(i), pol) : ld_u32_hint(cin + 4 * uint64_t(i), pol);
-        if (!step_checked(bits, active)) return false;
+        enc_step<DT, S>(st, bits, active, table_s, gwords, lt);
+        if (S == Sink::Count && hdr_bytes + 2u * uint32_t(-st.pos) >= n_c) return false;
     }
+    return true;
+}
+
+// Fast path for a full chunk: exponent bytes from the warp's slot, words
+// written backwards from the slot's end (st.pos: u16 index, counting down).
+// The word store of step j is issued after the state update of step j + 2:
+// its address depends on the ballots of all earlier steps, and a warp issues
+// in order, so storing at once would hold back every later step.  Returns
+// false, before any word could overwrite an exponent byte not yet read, if the
+// stream grows faster than the exponents are consumed.
+__device__ __forceinline__ uint32_t ld_slot_u8(const uint8_t* p) {
+    uint32_t v;
+    asm volatile("ld.global.cg.u8 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_slot_u16(uint8_t* p, uint32_t v) {
+    asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"(static_cast<unsigned short>(v)) : "memory");
+}
+
+__device__ bool encode_slot(uint8_t* slot, uint32_t table_s, uint32_t lane, EncState& st) {
+    const uint32_t lt = lanemask_lt();
+    st.x = kRansL;
+    st.pos = int32_t(kSlotBytes / 2);
+    uint32_t va[32], vb[32];
+    auto load_ex = [&](uint32_t (&v)[32], int32_t t) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = ld_slot_u8(slot + (uint32_t(t - j) * 32 + lane));
+    };
+    // exponent bytes of the block three ahead are pulled into L2 (8 lines)
+    auto prefetch_block = [&](int32_t t_top) {
+        const int32_t t_low = t_top - 31;
+        if (t_low >= 0 && lane < 8) asm volatile("prefetch.global.L2 [%0];" ::"l"(slot + uint32_t(t_low) * 32 + 128 * lane));
+    };
+    uint32_t w1 = 0, w2 = 0, b1 = 0, b2 = 0;
+    bool e1 = false, e2 = false;
+    auto flush_one = [&](uint32_t w, bool emit, uint32_t b) {
+        const int32_t nt = __popc(b);
+        if (emit) st_slot_u16(slot + 2u * uint32_t(st.pos - nt + __popc(b & lt)), w);
+        st.pos -= nt;
+    };
+    // Words stored during the block starting at step t0 (the two delayed
+    // steps of the last block and 30 of this one: at most 1024 words) must
+    // land on exponent bytes whose loads have surely completed.  Each store's
+    // address depends on the states of all steps before the previous block, so
+    // the bytes of steps above t0 + 32 qualify: u16 index 16 (t0 + 33) and up.
+    // Loads of later steps are in flight or not yet issued, and nothing orders
+    // them against another lane's store.
+    auto run_block = [&](const uint32_t (&v)[32], int32_t t0) -> bool {
+        if (st.pos - 32 * 32 < 16 * (t0 + 33)) return false;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const uint4 e = lds_table(table_s + 8 * v[j]);
+            const bool emit = st.x > e.z;
+            const uint32_t b = __ballot_sync(0xFFFFFFFFu, emit);
+            const uint32_t w = st.x;
+            st.x = rans_update(st.x, e, emit);
+            flush_one(w2, e2, b2);  // step j - 2
+            w2 = w1, e2 = e1, b2 = b1;
+            w1 = w, e1 = emit, b1 = b;
+        }
+        return true;
+    };
+    load_ex(va, int32_t(kSteps) - 1);
+    prefetch_block(int32_t(kSteps) - 65);
+    for (int32_t t0 = int32_t(kSteps) - 1;; t0 -= 64) {
+        load_ex(vb, t0 - 32);
+        prefetch_block(t0 - 96);
+        if (!run_block(va, t0)) return false;
+        const bool last = t0 == 63;
+        if (!last) load_ex(va, t0 - 64);
+        prefetch_block(t0 - 128);
+        if (!run_block(vb, t0 - 32)) return false;
+        if (last) break;
+    }
+    flush_one(w2, e2, b2);
+    flush_one(w1, e1, b1);
     return true;
 }
 
 // ---------------------------------------------------------------------------
 // output helpers
 
-// header of a coded stream: 32 states, bitmap, present frequencies ascending
-__device__ void write_stream_head_smem(uint8_t* dst, uint32_t x, const Norm& nm, uint32_t lane, const uint8_t* regB) {
-    uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);  // dst is 2-byte aligned
+// header of a coded stream, written to global memory (2-byte aligned): 32
+// states, bitmap, present frequencies ascending
+__device__ void write_stream_head(uint8_t* dst, uint32_t x, const Norm& nm, uint32_t lane, const uint8_t* regB) {
+    uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
     d16[2 * lane] = uint16_t(x);
     d16[2 * lane + 1] = uint16_t(x >> 16);
     if (lane < 16) d16[64 + lane] = uint16_t(regB[1536 + 2 * lane] | (regB[1536 + 2 * lane + 1] << 8));
@@ -540,36 +539,56 @@ __device__ void write_stream_head_smem(uint8_t* dst, uint32_t x, const Norm& nm,
         if (nm.present & (1u << k)) d16[80 + idx++] = uint16_t(nm.f[k]);
 }
 
-// copy `len` bytes from shared (2-byte aligned, ending at `end`) to global
-// (16-byte aligned), zero padding the last 16-byte block.
-__device__ void copy_record_out(const uint8_t* src, uint32_t len, const uint8_t* end, uint8_t* dst, uint32_t lane,
-                                uint64_t pol) {
+// Copies the record [start, kSlotBytes) of a slot (start 2-byte aligned) to dst
+// (16-byte aligned) in 16-byte blocks, zero padding the last block; 4
+// blocks in flight per lane.
+__device__ void copy_record_from_slot(const uint8_t* slot, uint32_t start, uint8_t* dst, uint32_t lane,
+                                      uint64_t pol) {
+    const uint32_t len = kSlotBytes - start;
     const uint32_t nb = (len + 15) / 16;
-    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src);
-    const uint32_t mis = uint32_t(s0 & 3u);  // 0 or 2
-    for (uint32_t b = lane; b < nb; b += 32) {
-        const uint8_t* sb = src + 16 * b;
-        const uint32_t* wp = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(sb) & ~uintptr_t(3));
-        uint32_t w[5];
+    const uint32_t mis = start & 2u;  // start mod 4 is 0 or 2
+    const uint32_t* wbase = reinterpret_cast<const uint32_t*>(slot + (start & ~3u));
+    const uint32_t nwords = (kSlotBytes - (start & ~3u)) / 4;  // words of the slot from wbase on
+    for (uint32_t b0 = 0; b0 < nb; b0 += 4 * 32) {
+        uint32_t w[4][5];
 #pragma unroll
-        for (int j = 0; j < 5; ++j) {
-            const uint8_t* a = reinterpret_cast<const uint8_t*>(wp + j);
-            w[j] = a < end ? wp[j] : 0u;
-        }
-        uint32_t o[4];
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t b = b0 + 32 * k + lane;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[j] = mis ? __byte_perm(w[j], w[j + 1], 0x5432) : w[j];
-        const uint32_t valid = len - 16 * b;  // bytes of this block inside the record
-        if (valid < 16) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t lo = 4 * j;
-                if (valid <= lo) o[j] = 0;
-                else if (valid < lo + 4) o[j] &= (1u << (8 * (valid - lo))) - 1u;
+            for (int j = 0; j < 5; ++j) {
+                const uint32_t wi = 4 * b + j;
+                w[k][j] = (b < nb && wi < nwords) ? __ldcg(wbase + wi) : 0u;
             }
         }
-        st_v4_hint(dst + 16 * b, make_uint4(o[0], o[1], o[2], o[3]), pol);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t b = b0 + 32 * k + lane;
+            if (b >= nb) continue;
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[j] = mis ? __byte_perm(w[k][j], w[k][j + 1], 0x5432) : w[k][j];
+            const uint32_t valid = len - 16 * b;
+            if (valid < 16) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t lo = 4 * j;
+                    if (valid <= lo) o[j] = 0;
+                    else if (valid < lo + 4) o[j] &= (1u << (8 * (valid - lo))) - 1u;
+                }
+            }
+            st_v4_hint(dst + 16 * b, make_uint4(o[0], o[1], o[2], o[3]), pol);
+        }
     }
+}
+
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+// drop the slot's L2 lines [first_byte, last_byte) (128-byte granularity,
+// lines partly outside the range are kept)
+__device__ void discard_slot(uint8_t* slot, uint32_t first_byte, uint32_t last_byte, uint32_t lane) {
+    const uint32_t l0 = (first_byte + 127) / 128, l1 = last_byte / 128;
+    for (uint32_t l = l0 + lane; l < l1; l += 32) discard_l2_line(slot + 128 * l);
 }
 
 // RAW chunk: the n_c exponent bytes, zero padded to 16
@@ -685,10 +704,6 @@ __device__ bool resolve_offset(uint64_t* desc, uint32_t c, uint64_t padded, uint
 }
 
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void discard_l2_line(const void* p) {
-    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
-}
-
 template <int DT>
 __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -704,8 +719,10 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
     const uint64_t pol_keep = policy_evict_last();
     const uint64_t pol_stream = policy_evict_first();
     const uint32_t processed = C - a.first_ticket;
-    // this warp's stash slot (one warp per block)
-    uint8_t* stash = a.stash ? a.stash + uint64_t(blockIdx.x) * kStashSlot : nullptr;
+    const uint32_t table_s = smem_addr(regA);
+    // this warp's two slots (one warp per block)
+    uint8_t* slots = a.stash ? a.stash + uint64_t(blockIdx.x) * 2 * kSlotBytes : nullptr;
+    uint32_t which = 0;
 
     // Chunk c is placed: table entries, done counter; the warp that completes
     // the last chunk writes the header.  Returns true for that warp.
@@ -750,38 +767,21 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
         return true;
     };
 
-    // A stashed chunk (coded, staged): its 16-byte aligned, zero padded record
-    // waits in the stash slot; once its offset is known it is copied out and
-    // the slot's L2 lines are dropped without write-back.
+    // A pending chunk: its record [p_start, kSlotBytes) waits in slot p_slot until
+    // its offset is known; then it is copied out and the slot's lines dropped.
     bool pend = false;
-    uint32_t p_c = 0, p_len = 0;
+    uint32_t p_c = 0, p_start = 0;
+    uint8_t* p_slot = nullptr;
     auto place_pending = [&]() -> bool {
+        const uint32_t len = kSlotBytes - p_start;
         uint64_t excl = 0;
-        const bool ok = resolve_offset(a.desc, p_c, round16(p_len), lane, excl);
-        if (ok) {
-            // 16-byte blocks, 8 loads in flight per lane before their stores
-            const uint32_t nb = (p_len + 15) / 16;
-            uint8_t* dst = a.out + exp_off + excl;
-            const uint4* src = reinterpret_cast<const uint4*>(stash);
-            for (uint32_t b0 = 0; b0 < nb; b0 += 8 * 32) {
-                uint4 v[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t b = b0 + 32 * k + lane;
-                    if (b < nb) v[k] = __ldcg(src + b);
-                }
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t b = b0 + 32 * k + lane;
-                    if (b < nb) st_v4_hint(dst + 16 * b, v[k], pol_stream);
-                }
-            }
-        }
+        const bool ok = resolve_offset(a.desc, p_c, round16(len), lane, excl);
+        if (ok) copy_record_from_slot(p_slot, p_start, a.out + exp_off + excl, lane, pol_stream);
         __syncwarp();
-        for (uint32_t l = lane; l < (p_len + 127) / 128; l += 32) discard_l2_line(stash + 128 * l);
+        discard_slot(p_slot, 0, kSlotBytes, lane);
         __syncwarp();
         pend = false;
-        return complete(p_c, p_len, false, excl, ok);
+        return complete(p_c, len, false, excl, ok);
     };
 
     uint32_t* ticket = &a.scratch->ticket;
@@ -793,9 +793,11 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
         const uint64_t left = n - uint64_t(c) * kChunk;
         const uint32_t n_c = uint32_t(left < kChunk ? left : kChunk);
         const uint8_t* cin = a.in + uint64_t(c) * kChunk * es;
+        uint8_t* slot = slots ? slots + which * kSlotBytes : nullptr;
 
-        // 1. plane split + histogram
-        split_and_count<DT>(cin, n_c, a.out + rem_off + uint64_t(c) * kChunk * rb, regA, lane, pol_keep, pol_stream);
+        // 1. plane split + exponent bytes + histogram
+        split_and_count<DT>(cin, n_c, a.out + rem_off + uint64_t(c) * kChunk * rb, slot, regA, lane, pol_keep,
+                            pol_stream);
         uint32_t cnt[8];
         reduce_hist(regA, lane, cnt);
         __syncwarp();
@@ -805,45 +807,38 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
         build_enc_table(nm, lane, regA, regB);
         const uint32_t hdr = kStreamHead + 2 * nm.k_total;
 
-        // 3. encode into shared staging
-        const uint32_t regA_s = smem_addr(regA);
-        EncState es_smem{kRansL, int32_t(kRegionA / 2)};
-        const int32_t limit = int32_t((kStageBase + hdr) / 2);
-        const bool fits =
-            encode_chunk<DT, Sink::Smem>(cin, n_c, regA_s, regA_s, lane, es_smem, limit, nullptr, hdr, pol_stream);
-        const uint32_t x = es_smem.x;
-        const int32_t pos = es_smem.pos;
-
-        uint32_t len = 0;
+        // 3. encode: fast path from the slot, else count from the input
+        EncState st{kRansL, 0};
+        bool fast = slot != nullptr && n_c == kChunk && encode_slot(slot, table_s, lane, st);
+        uint32_t len = 0, w_total = 0;
         bool raw = false;
-        uint32_t w_total = 0;
-        if (fits) {
-            w_total = kRegionA / 2 - uint32_t(pos);
+        if (fast) {
+            w_total = kSlotBytes / 2 - uint32_t(st.pos);
             len = hdr + 2 * w_total;
             raw = len >= n_c;
         } else {
-            EncState es_count{kRansL, 0};
-            const bool coded =
-                encode_chunk<DT, Sink::Count>(cin, n_c, regA_s, regA_s, lane, es_count, 0, nullptr, hdr, pol_stream);
-            w_total = uint32_t(-es_count.pos);
+            EncState cs{kRansL, 0};
+            const bool coded = encode_chunk<DT, Sink::Count>(cin, n_c, table_s, lane, cs, nullptr, hdr, pol_stream);
+            w_total = uint32_t(-cs.pos);
             len = hdr + 2 * w_total;
             raw = !coded || len >= n_c;
         }
         if (raw) len = n_c;
 
-        // 4. publish the length; place the previous stashed chunk, whose
+        // 4. publish the length; place the previous pending chunk, whose
         //    predecessors have had a whole chunk's time to finish
         publish_length(a.desc, c, round16(len), lane);
         if (pend && place_pending()) return;
-        if (stash && fits && !raw) {
-            uint8_t* rec = regA + 2 * uint32_t(pos) - hdr;
-            write_stream_head_smem(rec, x, nm, lane, regB);
+        if (fast && !raw) {
+            const uint32_t start = kSlotBytes - len;  // record = head + words, ending at the slot's end
+            write_stream_head(slot + start, st.x, nm, lane, regB);
             __syncwarp();
-            copy_record_out(rec, len, regA + kRegionA, stash, lane, pol_keep);
-            __syncwarp();
+            discard_slot(slot, 0, start, lane);  // exponent bytes below the record are spent
             pend = true;
             p_c = c;
-            p_len = len;
+            p_start = start;
+            p_slot = slot;
+            which ^= 1;
             continue;
         }
         // 5. otherwise place this chunk now
@@ -853,24 +848,16 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
             uint8_t* dst = a.out + exp_off + excl;
             if (raw) {
                 write_raw<DT>(cin, n_c, dst, lane);
-            } else if (fits) {
-                uint8_t* rec = regA + 2 * uint32_t(pos) - hdr;
-                write_stream_head_smem(rec, x, nm, lane, regB);
-                __syncwarp();
-                copy_record_out(rec, len, regA + kRegionA, dst, lane, pol_stream);
             } else {
-                // re-encode, writing the words in place behind the stream head
-                EncState es_glob{kRansL, int32_t(w_total)};
-                encode_chunk<DT, Sink::Global>(cin, n_c, regA_s, regA_s, lane, es_glob, 0, dst + hdr, hdr, pol_stream);
-                uint8_t* rec = regA + kStageBase;  // staging is free now: build the head there
-                write_stream_head_smem(rec, es_glob.x, nm, lane, regB);
-                __syncwarp();
-                for (uint32_t i = lane; i < hdr / 2; i += 32)
-                    reinterpret_cast<uint16_t*>(dst)[i] = reinterpret_cast<const uint16_t*>(rec)[i];
+                // encode again from the input, writing the words in place
+                EncState gs{kRansL, int32_t(w_total)};
+                encode_chunk<DT, Sink::Global>(cin, n_c, table_s, lane, gs, dst + hdr, hdr, pol_stream);
+                write_stream_head(dst, gs.x, nm, lane, regB);
                 for (uint32_t i = len + lane; i < round16(len); i += 32) dst[i] = 0;
             }
         }
         __syncwarp();
+        if (slot) discard_slot(slot, 0, kSlotBytes, lane);
         if (complete(c, len, raw, excl, ok)) return;
     }
     if (pend && place_pending()) return;
@@ -927,13 +914,13 @@ cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n
     uint64_t grid = uint64_t(per_sm) * uint64_t(sms);
     const uint64_t work = C > a.first_ticket ? C - a.first_ticket : 1;
     if (grid > work) grid = work;
-    if (stash && grid > stash_slots(n)) grid = stash_slots(n);  // one stash slot per warp
+    if (stash && grid > stash_warps(n)) grid = stash_warps(n);  // two slots per warp
     if (grid < 1) grid = 1;
     kern<<<dim3(uint32_t(grid)), dim3(32), kCompressSmem, s>>>(a);
     return cudaGetLastError();
 }
 
-// The regular path: the work area (counters, descriptors, stash) sits in the
+// The regular path: the work area (counters, descriptors, slots) sits in the
 // caller's output buffer, behind the largest possible container.
 cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                             int32_t* d_status, uint32_t first_ticket, cudaStream_t s) {

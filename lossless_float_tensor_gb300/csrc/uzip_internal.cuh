@@ -49,19 +49,23 @@ constexpr uint64_t kScratchHead = 16;
 __host__ __device__ inline uint64_t scratch_offset(int dtype, uint64_t n) { return round16(container_bound(dtype, n)); }
 // status, ticket, done counter and look-back descriptors (zeroed before each launch)
 __host__ __device__ inline uint64_t scratch_bytes(uint64_t n) { return kScratchHead + 8 * num_chunks(n); }
-// Stash: one 64 KiB slot per resident warp (at most kStashSlots warps), where a
-// chunk's finished stream waits for its offset while the warp moves on.  It is
-// never read before it is written.
-constexpr uint64_t kStashSlots = 2048;
-constexpr uint64_t kStashSlot = 65536;
-__host__ __device__ inline uint64_t stash_slots(uint64_t n) {
+// Slots: two slots of kSlotBytes per resident warp (at most kStashWarps
+// warps), used in turn.  A full chunk's exponent bytes fill the first 64 KiB
+// of a slot; its rANS words grow downwards from the slot's end, so the 4 KiB
+// beyond the exponent bytes keep the first words clear of bytes not yet read.
+// The finished stream then waits at the slot's end for its offset while the
+// warp counts its next chunk in the other slot.  Slots are never read before
+// they are written.
+constexpr uint64_t kStashWarps = 1536;
+constexpr uint32_t kSlotBytes = 65536 + 4096;
+__host__ __device__ inline uint64_t stash_warps(uint64_t n) {
     const uint64_t c = num_chunks(n);
-    return c < kStashSlots ? c : kStashSlots;
+    return c < kStashWarps ? c : kStashWarps;
 }
-// The stash starts at the first 256-byte aligned address (absolute) after the
+// The slots start at the first 256-byte aligned address (absolute) after the
 // descriptors; 256 bytes of slack cover the alignment.
 __host__ __device__ inline uint64_t work_area_bytes(uint64_t n) {
-    return scratch_bytes(n) + 256 + stash_slots(n) * kStashSlot;
+    return scratch_bytes(n) + 256 + stash_warps(n) * 2 * uint64_t(kSlotBytes);
 }
 
 // look-back descriptor: flag in bits 62..63, byte count in bits 0..61
@@ -70,12 +74,11 @@ constexpr uint64_t kDescInclusive = 2ull << 62;
 constexpr uint64_t kDescValue = (1ull << 62) - 1;
 
 // ---- compressor shared-memory plan (one warp per CTA) ---------------------
-// region A (32 KiB): phase 1 lane-private histogram u32[256][32];
-//                    phase 2 encode table (4 KiB) then word staging.
-// region B (2 KiB) : counts, frequencies, bitmap, present-symbol list.
-constexpr uint32_t kRegionA = 32768;
-constexpr uint32_t kEncTable = 4096;        // 256 x 16 bytes
-constexpr uint32_t kStageBase = kEncTable;  // staging occupies [kStageBase, kRegionA)
+// region A (16 KiB): lane-private histogram u32[256][16], then the encode
+//                    table (4 KiB: {m, add} rows at 0, {bound, packed} at 2 KiB)
+// region B (2 KiB) : frequencies, sort keys, bitmap, present-symbol list.
+constexpr uint32_t kRegionA = 16384;
+constexpr uint32_t kEncTable = 4096;
 constexpr uint32_t kRegionB = 2048;
 constexpr uint32_t kCompressSmem = kRegionA + kRegionB;
 

@@ -48,7 +48,7 @@ def test_max_compressed_size_is_container_bound_plus_work_area(uz):
             bound = oracle.container_bound(dtype, n)
             off = uz.library().uzip_debug_scratch_offset(dtype, n)
             assert off == -(-bound // 16) * 16
-            work = 16 + 8 * c + 256 + min(c, 2048) * 65536  # counters, descriptors, stash
+            work = 16 + 8 * c + 256 + min(c, 1536) * 2 * (65536 + 4096)  # counters, descriptors, two slots per warp
             assert uz.uzip_max_compressed_size(dtype, n) == off + work
     assert uz.uzip_max_compressed_size(7, 10) == 0
     assert uz.uzip_max_compressed_size(0, (1 << 40) + 1) == 0

@@ -61,6 +61,26 @@ def test_constant_and_random_chunks():
     assert not (lens[2] & 0x80000000) and (lens[2] & 0x7FFFFFFF) > 28 * 1024
 
 
+def test_chunks_whose_tail_outgrows_the_slot():
+    """Chunks coded from a slot's exponent bytes fall back to coding from the
+    input when the words written from the chunk's end would outrun the bytes
+    consumed: a constant chunk whose last 3072 values have random exponents
+    (about 12 bits each), the same with the noise in the middle (the fast path
+    holds), and a chunk of random bits ending in a constant run."""
+    rng = np.random.default_rng(33)
+    noisy_tail = np.full(65536, 0x3F80, np.uint16)
+    noisy_tail[-3072:] = (rng.integers(0, 256, 3072) << 7).astype(np.uint16)
+    noisy_mid = np.full(65536, 0x3F80, np.uint16)
+    noisy_mid[30000:33072] = (rng.integers(0, 256, 3072) << 7).astype(np.uint16)
+    random_then_const = rng.integers(0, 1 << 16, 65536).astype(np.uint16)
+    random_then_const[-5000:] = 0x4000
+    bits = np.concatenate([noisy_tail, noisy_mid, random_then_const, noisy_tail])
+    comp = _parity(bits)
+    lens = comp[64 + 8 * 4:64 + 12 * 4].view(np.uint32)
+    assert not (lens[0] & 0x80000000) and lens[0] == lens[3]
+    assert not (lens[1] & 0x80000000)
+
+
 def test_all_bf16_patterns_and_fp32_specials():
     x = np.arange(65536 * 3, dtype=np.uint32).astype(np.uint16)
     _parity(x)
