@@ -37,6 +37,14 @@ __device__ __forceinline__ uint32_t merge_bits(uint32_t e, uint32_t r) {
     if (DT == UZIP_BF16) return ((r & 0x80u) << 8) | (e << 7) | (r & 0x7Fu);
     return ((r & 0x800000u) << 8) | (e << 23) | (r & 0x7FFFFFu);
 }
+// The same merge for the decode loop, with fewer logic-unit instructions:
+// r * 257 puts the remainder byte at bits 0..7 and again at 8..15, so one
+// mask keeps the fraction (bits 0..6) and the sign (bit 15).
+template <int DT>
+__device__ __forceinline__ uint32_t merge_fast(uint32_t e, uint32_t r) {
+    if (DT == UZIP_BF16) return ((r * 257u) & 0x807Fu) | (e << 7);
+    return ((r & 0x7FFFFFu) | (e << 23)) | ((r << 8) & 0x80000000u);
+}
 
 template <int DT>
 __device__ void merge_raw(const uint8_t* __restrict__ ex, const uint8_t* __restrict__ rem, uint8_t* __restrict__ out,
@@ -101,8 +109,8 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
                              uint8_t* __restrict__ out, uint32_t n_c, uint32_t lane, uint8_t* wsm) {
     constexpr uint32_t es = DT == UZIP_BF16 ? 2 : 4;
     uint8_t* slot_sym = wsm;                                                   // u8[4096]
-    uint32_t* sym_fc = reinterpret_cast<uint32_t*>(wsm + kDecSlotTable);       // u32[256]: f | cum << 16
-    uint32_t* plist = reinterpret_cast<uint32_t*>(wsm + kDecSlotTable + 1024); // u32[256]: cum << 8 | s
+    uint2* sym_gc = reinterpret_cast<uint2*>(wsm + kDecSlotTable);                  // {f - 4096, -cum}
+    uint32_t* plist = reinterpret_cast<uint32_t*>(wsm + kDecSlotTable + kDecSymTable); // u32[256]: cum << 8 | s
     if (len < kStreamHead) return false;
     uint32_t x = reinterpret_cast<const uint32_t*>(src)[lane];
     const uint32_t bm = src[128 + lane];  // present symbols 8*lane .. 8*lane+7
@@ -133,7 +141,7 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             if (bm & (1u << k)) {
-                sym_fc[8 * lane + k] = f[k] | (cum << 16);
+                sym_gc[8 * lane + k] = make_uint2(f[k] - kM, 0u - cum);
                 plist[idx++] = (cum << 8) | (8 * lane + k);
             }
             cum += f[k];
@@ -183,7 +191,7 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
     const uint32_t wlast = W ? W - 1 : 0;
     const uint32_t lt = lanemask_lt();
     const uint32_t slot_s = static_cast<uint32_t>(__cvta_generic_to_shared(slot_sym));
-    const uint32_t fc_s = static_cast<uint32_t>(__cvta_generic_to_shared(sym_fc));
+    const uint32_t gc_s = static_cast<uint32_t>(__cvta_generic_to_shared(sym_gc));
     uint32_t pos = 0;
     // One decode step (rule R6, read side).  At most 32 words are consumed
     // per step, so every lane first fetches the word at pos + lane (pos is
@@ -191,20 +199,24 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
     // chain) and a lane that renormalises takes its word from lane
     // popc(ballot & lanes below) with one shuffle.  Reads past the stream
     // return some other word and leave pos > W, which fails the check after
-    // the loop.
-    auto step = [&](uint32_t t, uint32_t r, bool active, uint32_t win) {
+    // the loop.  The state update f (x >> 12) + (x mod 4096) - cum is computed
+    // as (x >> 12)(f - 4096) + x - cum (exact modulo 2^32, and the result is
+    // below 2^32), so one table entry {f - 4096, -cum} feeds it directly.
+    // `cur` advances by scale words per consumed word (the ring path keeps
+    // a per-lane byte cursor, the others the word position).
+    auto step = [&](uint32_t t, uint32_t r, bool active, uint32_t win, uint32_t& cur, uint32_t scale) {
         const uint32_t slot = x & (kM - 1);
-        uint32_t s, fc;
+        uint32_t s, g, nc;
         asm("ld.shared.u8 %0, [%1];" : "=r"(s) : "r"(slot_s + slot));
-        asm("ld.shared.u32 %0, [%1];" : "=r"(fc) : "r"(fc_s + 4 * s));
-        const uint32_t xn = (fc & 0xFFFFu) * (x >> kProbBits) + slot - (fc >> 16);
+        asm("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(g), "=r"(nc) : "r"(gc_s + 8 * s));
+        const uint32_t xn = (x >> kProbBits) * g + x + nc;
         const bool need = active && xn < kRansL;
         const uint32_t b = __ballot_sync(0xFFFFFFFFu, need);
         const uint32_t w = __shfl_sync(0xFFFFFFFFu, win, __popc(b & lt));
-        pos += __popc(b);
+        cur += scale * __popc(b);
         if (active) {
             x = need ? ((xn << 16) | w) : xn;
-            const uint32_t v = merge_bits<DT>(s, r);
+            const uint32_t v = merge_fast<DT>(s, r);
             const uint64_t i = 32 * uint64_t(t) + lane;
             if (es == 2) reinterpret_cast<uint16_t*>(out)[i] = uint16_t(v);
             else reinterpret_cast<uint32_t*>(out)[i] = v;
@@ -214,12 +226,15 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
         const uint32_t widx = pos + lane;
         return __ldg(words + (widx < wlast ? widx : wlast));
     };
+    auto load_rem_full = [&](uint32_t t) -> uint32_t {  // t < 2048 of a full chunk
+        const uint32_t i = 32 * t + lane;
+        if (DT == UZIP_BF16) return __ldg(rem + i);
+        return uint32_t(__ldg(rem + 3 * i)) | uint32_t(__ldg(rem + 3 * i + 1)) << 8 | uint32_t(__ldg(rem + 3 * i + 2)) << 16;
+    };
     auto load_rem = [&](uint32_t t) -> uint32_t {
         const uint32_t i = 32 * t + lane;
         if (i >= n_c) return 0;
-        if (DT == UZIP_BF16) return __ldg(rem + i);
-        return uint32_t(__ldg(rem + 3 * uint64_t(i))) | uint32_t(__ldg(rem + 3 * uint64_t(i) + 1)) << 8 |
-               uint32_t(__ldg(rem + 3 * uint64_t(i) + 2)) << 16;
+        return load_rem_full(t);
     };
     if (n_c == kChunk && RING) {
         // Word stream staged in a 1 KiB ring (the present-symbol list is no
@@ -249,9 +264,13 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
         uint4 pend = make_uint4(0, 0, 0, 0);
         uint32_t pend_piece = 0;
         bool has_pend = false;
+        // per-lane byte cursor: offset in the record of word pos + lane
+        const uint32_t lane_off = wb0 + 2 * lane;
+        uint32_t rq = lane_off;
         auto top_up = [&]() {
             if (has_pend) store_piece(pend_piece, pend);
             has_pend = false;
+            pos = (rq - lane_off) >> 1;
             const uint32_t cur = (wb0 + 2 * pos) >> 8;
             uint32_t need_end = ((wb0 + 2 * (pos + 8 * 32)) >> 8) + 1;
             need_end = need_end < npieces ? need_end : npieces;
@@ -269,8 +288,8 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
         };
         auto rwin = [&]() -> uint32_t {
             uint32_t v;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(*reinterpret_cast<unsigned short*>(&v)) : "r"(ring_s + ((wb0 + 2 * (pos + lane)) & 1023u)) : "memory");
-            return v & 0xFFFFu;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(ring_s + (rq & 1023u)) : "memory");
+            return v;
         };
         // Both streams are cold in L2 when decompression starts: pull the
         // remainder bytes of the steps 64 ahead and the stream bytes ~1 KiB
@@ -281,32 +300,33 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
             if (lane < kRemLines && t_ahead + 16 <= kSteps)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(rem + uint64_t(t_ahead) * 32 * rb + 128 * lane));
             if (lane >= 30) {
-                const uint32_t at = wb0 + 2 * pos + 1024 + 128 * (lane - 30);
+                const uint32_t at = (rq - 2 * lane) + 1024 + 128 * (lane - 30);
                 if (at < nlines * 16) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + at));
             }
         };
         constexpr int PF = 8;
         uint32_t ra[PF], rbk[PF];
 #pragma unroll
-        for (int j = 0; j < PF; ++j) ra[j] = load_rem(j);
+        for (int j = 0; j < PF; ++j) ra[j] = load_rem_full(j);
         prefetch_l2(16);
         prefetch_l2(32);
         prefetch_l2(48);
         for (uint32_t t0 = 0; t0 < kSteps; t0 += 2 * PF) {
             prefetch_l2(t0 + 64);
 #pragma unroll
-            for (int j = 0; j < PF; ++j) rbk[j] = load_rem(t0 + PF + j);
+            for (int j = 0; j < PF; ++j) rbk[j] = load_rem_full(t0 + PF + j);
             top_up();
 #pragma unroll
-            for (int j = 0; j < PF; ++j) step(t0 + j, ra[j], true, rwin());
+            for (int j = 0; j < PF; ++j) step(t0 + j, ra[j], true, rwin(), rq, 2);
             if (t0 + 2 * PF < kSteps) {
 #pragma unroll
-                for (int j = 0; j < PF; ++j) ra[j] = load_rem(t0 + 2 * PF + j);
+                for (int j = 0; j < PF; ++j) ra[j] = load_rem_full(t0 + 2 * PF + j);
             }
             top_up();
 #pragma unroll
-            for (int j = 0; j < PF; ++j) step(t0 + PF + j, rbk[j], true, rwin());
+            for (int j = 0; j < PF; ++j) step(t0 + PF + j, rbk[j], true, rwin(), rq, 2);
         }
+        pos = (rq - lane_off) >> 1;
     } else if (n_c == kChunk) {
         // The word stream is read sequentially, ~11 bytes per step: pull the
         // lines about 40 steps ahead into L1 so a step never waits on a first
@@ -323,24 +343,24 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
         constexpr int PF = DT == UZIP_BF16 ? 16 : 8;
         uint32_t ra[PF], rbk[PF];
 #pragma unroll
-        for (int j = 0; j < PF; ++j) ra[j] = load_rem(j);
+        for (int j = 0; j < PF; ++j) ra[j] = load_rem_full(j);
         for (uint32_t t0 = 0; t0 < kSteps; t0 += 2 * PF) {
             prefetch_words();
 #pragma unroll
-            for (int j = 0; j < PF; ++j) rbk[j] = load_rem(t0 + PF + j);
+            for (int j = 0; j < PF; ++j) rbk[j] = load_rem_full(t0 + PF + j);
 #pragma unroll
-            for (int j = 0; j < PF; ++j) step(t0 + j, ra[j], true, gwin());
+            for (int j = 0; j < PF; ++j) step(t0 + j, ra[j], true, gwin(), pos, 1);
             if (DT == UZIP_BF16) prefetch_words();
             if (t0 + 2 * PF < kSteps) {
 #pragma unroll
-                for (int j = 0; j < PF; ++j) ra[j] = load_rem(t0 + 2 * PF + j);
+                for (int j = 0; j < PF; ++j) ra[j] = load_rem_full(t0 + 2 * PF + j);
             }
 #pragma unroll
-            for (int j = 0; j < PF; ++j) step(t0 + PF + j, rbk[j], true, gwin());
+            for (int j = 0; j < PF; ++j) step(t0 + PF + j, rbk[j], true, gwin(), pos, 1);
         }
     } else {
         const uint32_t T = (n_c + 31) / 32;
-        for (uint32_t t = 0; t < T; ++t) step(t, load_rem(t), 32 * t + lane < n_c, gwin());
+        for (uint32_t t = 0; t < T; ++t) step(t, load_rem(t), 32 * t + lane < n_c, gwin(), pos, 1);
     }
     const bool fail = bad || x != kRansL || pos != W;
     return !__any_sync(0xFFFFFFFFu, fail);
