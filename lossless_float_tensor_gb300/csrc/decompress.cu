@@ -367,7 +367,7 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kDecWarps * 32, 7) decompress_kernel(DecompressArgs a) {
+__global__ void __launch_bounds__(kDecWarps * 32, 28 / kDecWarps) decompress_kernel(DecompressArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const uint32_t lane = threadIdx.x & 31;
     const uint32_t wid = threadIdx.x >> 5;

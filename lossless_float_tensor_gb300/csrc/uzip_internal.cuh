@@ -87,7 +87,7 @@ constexpr uint32_t kCompressSmem = kRegionA + kRegionB;
 constexpr uint32_t kSpinLimit = 1u << 20;
 
 // ---- decompressor shared-memory plan (per warp) ---------------------------
-constexpr uint32_t kDecWarps = 4;
+constexpr uint32_t kDecWarps = 1;
 constexpr uint32_t kDecSlotTable = 4096;    // slot -> symbol, u8[4096]
 constexpr uint32_t kDecSymTable = 2048;     // symbol -> {f - 4096, -cum}, u32 pairs[256]
 constexpr uint32_t kDecList = 1024;         // present symbols, u32[256]: cum << 8 | symbol
