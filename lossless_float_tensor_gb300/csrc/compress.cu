@@ -633,6 +633,9 @@ __device__ void publish_length(uint64_t* desc, uint32_t c, uint64_t padded, uint
     if (lane == 0) st_release_u64(desc + c, (c == 0 ? kDescInclusive : kDescAggregate) | padded);
 }
 
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
     uint64_t v;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -653,6 +656,9 @@ __device__ bool resolve_offset(uint64_t* desc, uint32_t c, uint64_t padded, uint
     uint32_t spins = 0;
     uint32_t backoff = 32;
     bool ok = true;
+    uint64_t d0[4] = {0, 0, 0, 0};  // the nearest window, kept for helping
+    uint32_t first0 = 0, kin0 = 0;
+    bool first_round = true;
     while (true) {
         // lane l holds descriptors top - 4l .. top - 4l - 3 (k = 0 nearest)
         uint64_t d[4];
@@ -685,6 +691,13 @@ __device__ bool resolve_offset(uint64_t* desc, uint32_t c, uint64_t padded, uint
             backoff = backoff < 1024 ? backoff * 2 : 1024;
             continue;
         }
+        if (first_round) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) d0[k] = d[k];
+            first0 = first;
+            kin0 = kin;
+            first_round = false;
+        }
         uint64_t val = 0;
         if (lane < first) {
 #pragma unroll
@@ -699,6 +712,35 @@ __device__ bool resolve_offset(uint64_t* desc, uint32_t c, uint64_t padded, uint
         top -= 128;
     }
     if (lane == 0) st_release_u64(desc + c, kDescInclusive | ((excl + padded) & kDescValue));
+    // Help the chunks of the nearest window that had only aggregates: their
+    // inclusive prefixes follow from this one (excl minus the aggregates of
+    // the chunks between), and publishing them lets the next walks stop
+    // within one round trip.  A prefix is unique, so a chunk's own warp or
+    // another helper writing it too stores the same value.
+    if (ok && first0 > 0) {
+        const uint32_t nk = lane < first0 ? 4u : (lane == first0 ? kin0 : 0u);
+        uint64_t v[4], tot = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[k] = uint32_t(k) < nk ? (d0[k] & kDescValue) : 0;
+            tot += v[k];
+        }
+        uint64_t inc = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= uint32_t(o)) inc += t;
+        }
+        uint64_t between = inc - tot;  // aggregates of the chunks nearer than this lane's
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (uint32_t(k) < nk) {
+                const uint64_t idx = uint64_t(c) - 1 - 4 * lane - k;
+                st_relaxed_u64(desc + idx, kDescInclusive | ((excl - between) & kDescValue));
+            }
+            between += v[k];
+        }
+    }
     excl_out = excl;
     return ok;
 }
