@@ -183,10 +183,21 @@ const char* uzip_status_string(uzip_status st);
  *                            cudaMemcpyAsync of the size bound per message.
  *                            UZIP_PIPE_SERIAL: compress then copy on one
  *                            stream, no overlap (the naive design of UCCL-Zip
- *                            Fig. 1 a), for comparison.
+ *                            Fig. 1 a), for comparison.  UZIP_PIPE_SIZED:
+ *                            the host waits for each message's compression
+ *                            to finish, reads its size from h_sizes and
+ *                            issues one cudaMemcpyAsync of exactly that many
+ *                            bytes (the copy engine instead of SM stores; the
+ *                            call then blocks until the last compression has
+ *                            finished, while the copies still overlap it).
  * Returns once all work is enqueued; the work ends when both streams drain.
  * The caller must not reuse the banks until then. */
-typedef enum { UZIP_PIPE_EXACT = 0, UZIP_PIPE_BOUND = 1, UZIP_PIPE_SERIAL = 2 } uzip_pipe_mode;
+typedef enum {
+    UZIP_PIPE_EXACT = 0,
+    UZIP_PIPE_BOUND = 1,
+    UZIP_PIPE_SERIAL = 2,
+    UZIP_PIPE_SIZED = 3
+} uzip_pipe_mode;
 
 uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d_msgs, const uint64_t* msg_elems,
                                uint32_t n_msgs, void* const* d_bank, uint64_t bank_capacity,

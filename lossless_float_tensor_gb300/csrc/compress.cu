@@ -13,13 +13,12 @@
 //      before it (Merrill and Garland, "Single-pass parallel prefix scan with
 //      decoupled look-back", 2016) and, after its next chunk, copies the
 //      stream to its offset with 16-byte stores.
-// Each warp owns two 64 KiB slots used in turn, so a finished stream can wait
+// Each warp owns two 68 KiB slots used in turn, so a finished stream can wait
 // for its offset while the next chunk is counted.  A chunk whose words would
-// reach exponent bytes not yet read (over 4 bits per value), a partial last
-// chunk, and every chunk when no slots are given (the allocation-free entry
-// point) are encoded twice from the input instead: once counting, once
-// writing in place.  A chunk that coding does not shrink is stored RAW
-// (NCCLZ Sec. IV-C).
+// reach exponent bytes not yet read, and every chunk when no slots are given
+// (the allocation-free entry point), is encoded twice from the input instead:
+// once counting, once writing in place.  A chunk that coding does not shrink
+// is stored RAW (NCCLZ Sec. IV-C).
 #include <mutex>
 
 #include "uzip_internal.cuh"
@@ -447,8 +446,8 @@ __device__ bool encode_chunk(const uint8_t* __restrict__ cin, uint32_t n_c, uint
     return true;
 }
 
-// Fast path for a full chunk: exponent bytes from the warp's slot, words
-// written backwards from the slot's end (st.pos: u16 index, counting down).
+// Fast path: exponent bytes from the warp's slot, words written backwards
+// from the slot's end (st.pos: u16 index, counting down).
 // The word store of step j is issued after the state update of step j + 2:
 // its address depends on the ballots of all earlier steps, and a warp issues
 // in order, so storing at once would hold back every later step.  Returns
@@ -463,10 +462,28 @@ __device__ __forceinline__ void st_slot_u16(uint8_t* p, uint32_t v) {
     asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"(static_cast<unsigned short>(v)) : "memory");
 }
 
-__device__ bool encode_slot(uint8_t* slot, uint32_t table_s, uint32_t lane, EncState& st) {
+__device__ bool encode_slot(uint8_t* slot, uint32_t n_c, uint32_t table_s, uint32_t lane, EncState& st) {
     const uint32_t lt = lanemask_lt();
     st.x = kRansL;
     st.pos = int32_t(kSlotBytes / 2);
+    const int32_t T = int32_t((n_c + 31) / 32);  // steps
+    const int32_t T0 = int32_t(n_c / 32) & ~31;  // steps in whole 32-step blocks of full steps
+    // Steps above the whole blocks (a partial chunk only), one at a time: the
+    // top step may have lanes past the chunk's end, which neither update nor
+    // emit.  Their words go straight to the slot.
+    for (int32_t t = T - 1; t >= T0; --t) {
+        const bool active = uint32_t(t) * 32 + lane < n_c;
+        const uint32_t v = ld_slot_u8(slot + (uint32_t(t) * 32 + lane));
+        const uint4 e = lds_table(table_s + 8 * v);
+        const bool emit = active && st.x > e.z;
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, emit);
+        const int32_t nt = __popc(b);
+        if (emit) st_slot_u16(slot + 2u * uint32_t(st.pos - nt + __popc(b & lt)), st.x);
+        st.pos -= nt;
+        const uint32_t xn = rans_update(st.x, e, emit);
+        st.x = active ? xn : st.x;
+    }
+    if (T0 == 0) return true;
     uint32_t va[32], vb[32];
     auto load_ex = [&](uint32_t (&v)[32], int32_t t) {
 #pragma unroll
@@ -506,17 +523,21 @@ __device__ bool encode_slot(uint8_t* slot, uint32_t table_s, uint32_t lane, EncS
         }
         return true;
     };
-    load_ex(va, int32_t(kSteps) - 1);
-    prefetch_block(int32_t(kSteps) - 65);
-    for (int32_t t0 = int32_t(kSteps) - 1;; t0 -= 64) {
-        load_ex(vb, t0 - 32);
+    // whole blocks from step T0 - 1 down, two per iteration (the buffers
+    // alternate); an odd count ends with a single block
+    load_ex(va, T0 - 1);
+    prefetch_block(T0 - 65);
+    for (int32_t t0 = T0 - 1;; t0 -= 64) {
+        const bool has_b = t0 >= 63;
+        if (has_b) load_ex(vb, t0 - 32);
         prefetch_block(t0 - 96);
         if (!run_block(va, t0)) return false;
-        const bool last = t0 == 63;
-        if (!last) load_ex(va, t0 - 64);
+        if (!has_b) break;
+        const bool more = t0 >= 95;
+        if (more) load_ex(va, t0 - 64);
         prefetch_block(t0 - 128);
         if (!run_block(vb, t0 - 32)) return false;
-        if (last) break;
+        if (!more) break;
     }
     flush_one(w2, e2, b2);
     flush_one(w1, e1, b1);
@@ -851,7 +872,7 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
 
         // 3. encode: fast path from the slot, else count from the input
         EncState st{kRansL, 0};
-        bool fast = slot != nullptr && n_c == kChunk && encode_slot(slot, table_s, lane, st);
+        bool fast = slot != nullptr && encode_slot(slot, n_c, table_s, lane, st);
         uint32_t len = 0, w_total = 0;
         bool raw = false;
         if (fast) {

@@ -51,7 +51,8 @@ extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d
     using namespace uzip;
     if (dtype != UZIP_BF16 && dtype != UZIP_FP32) return UZIP_ERR_UNSUPPORTED_DTYPE;
     if (n_msgs == 0 || !d_msgs || !msg_elems || !d_bank || !h_bank || !h_sizes) return UZIP_ERR_INVALID_ARG;
-    if (mode != UZIP_PIPE_EXACT && mode != UZIP_PIPE_BOUND && mode != UZIP_PIPE_SERIAL) return UZIP_ERR_INVALID_ARG;
+    if (mode != UZIP_PIPE_EXACT && mode != UZIP_PIPE_BOUND && mode != UZIP_PIPE_SERIAL && mode != UZIP_PIPE_SIZED)
+        return UZIP_ERR_INVALID_ARG;
     uint64_t largest = 0;
     for (uint32_t k = 0; k < n_msgs; ++k) {
         if (msg_elems[k] > UZIP_MAX_ELEMS) return UZIP_ERR_INVALID_ARG;
@@ -95,10 +96,18 @@ extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d
             break;
         }
         cudaError_t err;
-        if (mode == UZIP_PIPE_BOUND)
+        if (mode == UZIP_PIPE_BOUND) {
             err = cudaMemcpyAsync(h_bank[b], d_bank[b], container_bound(dtype, msg_elems[k]), cudaMemcpyDeviceToHost, sx);
-        else
+        } else if (mode == UZIP_PIPE_SIZED) {
+            // the size is known once this compression is done; message k-1's
+            // copy keeps running on s_copy meanwhile
+            err = cudaEventSynchronize(compressed[b]);
+            const uint64_t total = *reinterpret_cast<volatile const uint64_t*>(h_sizes + k);
+            if (err == cudaSuccess && total > 0)
+                err = cudaMemcpyAsync(h_bank[b], d_bank[b], total, cudaMemcpyDeviceToHost, sx);
+        } else {
             err = launch_copy_exact(d_bank[b], h_dev[b], sx);
+        }
         if (err == cudaSuccess && !serial) err = cudaEventRecord(copied[b], sx);
         if (err != cudaSuccess) result = UZIP_ERR_CUDA;
     }

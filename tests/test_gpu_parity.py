@@ -180,7 +180,7 @@ def test_query_size():
     assert total == oracle.compress(bits).size
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
 def test_pipeline_send(mode):
     import torch
 
