@@ -22,7 +22,9 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "liboracle.so")
 SOURCES = [os.path.join(HERE, "uzip_oracle.c")]
 
-BF16, FP32 = 0, 1
+BF16, FP32, FP16, FP8_E4M3, FP8_E5M2 = 0, 1, 2, 3, 4
+ELEM_BYTES = {BF16: 2, FP32: 4, FP16: 2, FP8_E4M3: 1, FP8_E5M2: 1}
+BITS_DTYPE = {BF16: np.uint16, FP32: np.uint32, FP16: np.uint16, FP8_E4M3: np.uint8, FP8_E5M2: np.uint8}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DTYPE, ERR_CAPACITY, ERR_CORRUPT = 0, 1, 2, 3, 4
 CHUNK = 65536
 M = 4096
@@ -65,6 +67,8 @@ def lib():
         L.orc_decode_chunk.argtypes = [vp, ctypes.c_uint32, ctypes.c_int, ctypes.c_uint32, vp]
         L.orc_container_bound.argtypes = [ctypes.c_int, ctypes.c_uint64]
         L.orc_container_bound.restype = ctypes.c_uint64
+        L.orc_remainder_plane_bytes.argtypes = [ctypes.c_int, ctypes.c_uint64]
+        L.orc_remainder_plane_bytes.restype = ctypes.c_uint64
         L.orc_compress.argtypes = [ctypes.c_int, vp, ctypes.c_uint64, vp, ctypes.c_uint64, u64p]
         L.orc_decompress.argtypes = [vp, ctypes.c_uint64, ctypes.c_int, ctypes.c_uint64, vp]
         for name in ("orc_split", "orc_merge", "orc_normalise", "orc_rans_encode", "orc_rans_decode",
@@ -92,27 +96,43 @@ def _check(st: int, what: str):
 
 
 def dtype_code(a: np.ndarray) -> int:
-    """bf16 tensors travel as uint16 bit patterns, fp32 as uint32 or float32."""
+    """Container dtype implied by a numpy array: bf16 travels as uint16 bit
+    patterns, fp16 as float16, fp32 as uint32 or float32.  The fp8 formats
+    have no numpy type: pass dtype= explicitly with uint8 bit patterns."""
     if a.dtype in (np.uint16, np.int16):
         return BF16
+    if a.dtype == np.float16:
+        return FP16
     if a.dtype in (np.uint32, np.float32, np.int32):
         return FP32
     raise TypeError(f"no container dtype for numpy {a.dtype}")
 
 
-def split(bits: np.ndarray):
-    d = dtype_code(bits)
-    bits = np.ascontiguousarray(bits)
+def _bits(a: np.ndarray, dtype: int | None):
+    d = dtype_code(a) if dtype is None else dtype
+    a = np.ascontiguousarray(a).reshape(-1)
+    if a.dtype.itemsize != ELEM_BYTES[d]:
+        raise TypeError(f"{a.dtype} elements do not match dtype {d}")
+    return d, a.view(BITS_DTYPE[d])
+
+
+def remainder_plane_bytes(dtype: int, n: int) -> int:
+    return int(lib().orc_remainder_plane_bytes(dtype, n))
+
+
+def split(bits: np.ndarray, dtype: int | None = None):
+    d, bits = _bits(bits, dtype)
     n = bits.size
     exps = np.empty(n, np.uint8)
-    rem = np.empty(n * (1 if d == BF16 else 3), np.uint8)
-    _check(lib().orc_split(d, _ptr(bits), n, _ptr(exps), _ptr(rem)), "split")
-    return exps, rem
+    rem = np.empty(max(1, remainder_plane_bytes(d, n)), np.uint8)
+    _check(lib().orc_split(d, _ptr(bits if n else np.zeros(1, bits.dtype)), n, _ptr(exps if n else np.zeros(1, np.uint8)),
+                           _ptr(rem)), "split")
+    return exps, rem[: remainder_plane_bytes(d, n)]
 
 
 def merge(dtype: int, exps: np.ndarray, rem: np.ndarray) -> np.ndarray:
     n = exps.size
-    out = np.empty(n, np.uint16 if dtype == BF16 else np.uint32)
+    out = np.empty(n, BITS_DTYPE[dtype])
     _check(lib().orc_merge(dtype, _ptr(np.ascontiguousarray(exps)), _ptr(np.ascontiguousarray(rem)), n, _ptr(out)), "merge")
     return out
 
@@ -177,10 +197,10 @@ def container_bound(dtype: int, n: int) -> int:
     return int(lib().orc_container_bound(dtype, n))
 
 
-def compress(bits: np.ndarray) -> np.ndarray:
-    """Container bytes for a bf16 (uint16 bits) or fp32 (uint32/float32) array."""
-    d = dtype_code(bits)
-    bits = np.ascontiguousarray(bits).reshape(-1)
+def compress(bits: np.ndarray, dtype: int | None = None) -> np.ndarray:
+    """Container bytes for an array of element bit patterns (see dtype_code;
+    fp8 needs dtype=FP8_E4M3 or FP8_E5M2 with uint8 bits)."""
+    d, bits = _bits(bits, dtype)
     n = bits.size
     cap = container_bound(d, n)
     out = np.empty(max(cap, 1), np.uint8)
@@ -192,7 +212,7 @@ def compress(bits: np.ndarray) -> np.ndarray:
 
 def decompress_status(comp: np.ndarray, dtype: int, n: int):
     comp = np.ascontiguousarray(np.asarray(comp, np.uint8))
-    out = np.empty(max(1, n), np.uint16 if dtype == BF16 else np.uint32)
+    out = np.empty(max(1, n), BITS_DTYPE.get(dtype, np.uint32))  # unknown dtype: the oracle refuses it
     buf = comp if comp.size else np.zeros(1, np.uint8)
     st = lib().orc_decompress(_ptr(buf), comp.size, dtype, n, _ptr(out))
     return st, out[:n]

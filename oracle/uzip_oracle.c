@@ -43,63 +43,94 @@ static void wr_le(uint8_t* p, uint64_t v, int nbytes) {
 
 static uint64_t round16(uint64_t v) { return (v + 15u) / 16u * 16u; }
 
-static int remainder_bytes(int dtype) { return dtype == ORC_BF16 ? 1 : 3; }
-
 /* ------------------------------------------------------------------------ */
-/* R1: split each value into its exponent byte and its sign|fraction bits.  */
-/* bf16 = s | e(8) | m(7):  rem = s<<7 | m           (1 byte)              */
-/* fp32 = s | e(8) | m(23): rem = s<<23 | m          (3 bytes, LE)         */
+/* R1, R21, R22: split each value into its exponent field and its           */
+/* sign|fraction bits, the sign placed just above the fraction.             */
+/* bf16    = s | e(8) | m(7):  rem = s<<7 | m    (1 byte)                   */
+/* fp32    = s | e(8) | m(23): rem = s<<23 | m   (3 bytes, LE)              */
+/* fp16    = s | e(5) | m(10): rem = s<<10 | m   (2 bytes, LE)              */
+/* e4m3fn  = s | e(4) | m(3):  rem = s<<3 | m    (4 bits)                   */
+/* e5m2    = s | e(5) | m(2):  rem = s<<2 | m    (4 bits, top bit 0)        */
+/* The 4-bit fields of the fp8 formats are packed two per byte: element 2j */
+/* in the low nibble of byte j, element 2j+1 in the high nibble (a missing */
+/* last element leaves it zero).                                            */
+
+/* (exponent bits, fraction bits, element bytes) of each dtype */
+static int layout(int dtype, int* ebits, int* mbits, int* es) {
+    switch (dtype) {
+        case ORC_BF16: *ebits = 8; *mbits = 7; *es = 2; return 1;
+        case ORC_FP32: *ebits = 8; *mbits = 23; *es = 4; return 1;
+        case ORC_FP16: *ebits = 5; *mbits = 10; *es = 2; return 1;
+        case ORC_FP8_E4M3: *ebits = 4; *mbits = 3; *es = 1; return 1;
+        case ORC_FP8_E5M2: *ebits = 5; *mbits = 2; *es = 1; return 1;
+        default: return 0;
+    }
+}
+
+static int dtype_ok(int dtype) {
+    int eb, mb, es;
+    return layout(dtype, &eb, &mb, &es);
+}
+
+uint64_t orc_remainder_plane_bytes(int dtype, uint64_t n) {
+    switch (dtype) {
+        case ORC_BF16: return n;
+        case ORC_FP32: return 3 * n;
+        case ORC_FP16: return 2 * n;
+        case ORC_FP8_E4M3:
+        case ORC_FP8_E5M2: return (n + 1) / 2;
+        default: return 0;
+    }
+}
+
+/* remainder field of element i: read / write */
+static uint32_t get_rem(int dtype, const uint8_t* rem, uint64_t i) {
+    if (dtype == ORC_FP8_E4M3 || dtype == ORC_FP8_E5M2) return (rem[i / 2] >> (4 * (i % 2))) & 0xFu;
+    if (dtype == ORC_BF16) return rem[i];
+    if (dtype == ORC_FP16) return (uint32_t)rd_le(rem + 2 * i, 2);
+    return (uint32_t)rd_le(rem + 3 * i, 3);
+}
+
+static void put_rem(int dtype, uint8_t* rem, uint64_t i, uint32_t r) {
+    if (dtype == ORC_FP8_E4M3 || dtype == ORC_FP8_E5M2) {
+        if (i % 2 == 0) rem[i / 2] = (uint8_t)r; /* also clears the high nibble */
+        else rem[i / 2] = (uint8_t)(rem[i / 2] | (r << 4));
+        return;
+    }
+    if (dtype == ORC_BF16) rem[i] = (uint8_t)r;
+    else if (dtype == ORC_FP16) wr_le(rem + 2 * i, r, 2);
+    else wr_le(rem + 3 * i, r, 3);
+}
 
 int orc_split(int dtype, const void* in, uint64_t n, uint8_t* exps, uint8_t* rem) {
+    int ebits, mbits, es;
+    if (!layout(dtype, &ebits, &mbits, &es)) return ORC_ERR_UNSUPPORTED_DTYPE;
     const uint8_t* src = (const uint8_t*)in;
-    if (dtype == ORC_BF16) {
-        for (uint64_t i = 0; i < n; ++i) {
-            uint32_t bits = (uint32_t)rd_le(src + 2 * i, 2);
-            uint32_t sign = (bits >> 15) & 1u;
-            uint32_t e = (bits >> 7) & 0xFFu;
-            uint32_t m = bits & 0x7Fu;
-            exps[i] = (uint8_t)e;
-            rem[i] = (uint8_t)((sign << 7) | m);
-        }
-        return ORC_OK;
+    const int width = 8 * es;
+    for (uint64_t i = 0; i < n; ++i) {
+        uint32_t bits = (uint32_t)rd_le(src + (uint64_t)es * i, es);
+        uint32_t sign = (bits >> (width - 1)) & 1u;
+        uint32_t e = (bits >> mbits) & ((1u << ebits) - 1u);
+        uint32_t m = bits & ((1u << mbits) - 1u);
+        exps[i] = (uint8_t)e;
+        put_rem(dtype, rem, i, (sign << mbits) | m);
     }
-    if (dtype == ORC_FP32) {
-        for (uint64_t i = 0; i < n; ++i) {
-            uint32_t bits = (uint32_t)rd_le(src + 4 * i, 4);
-            uint32_t sign = (bits >> 31) & 1u;
-            uint32_t e = (bits >> 23) & 0xFFu;
-            uint32_t m = bits & 0x7FFFFFu;
-            exps[i] = (uint8_t)e;
-            wr_le(rem + 3 * i, ((uint64_t)sign << 23) | m, 3);
-        }
-        return ORC_OK;
-    }
-    return ORC_ERR_UNSUPPORTED_DTYPE;
+    return ORC_OK;
 }
 
 int orc_merge(int dtype, const uint8_t* exps, const uint8_t* rem, uint64_t n, void* out) {
+    int ebits, mbits, es;
+    if (!layout(dtype, &ebits, &mbits, &es)) return ORC_ERR_UNSUPPORTED_DTYPE;
     uint8_t* dst = (uint8_t*)out;
-    if (dtype == ORC_BF16) {
-        for (uint64_t i = 0; i < n; ++i) {
-            uint32_t r = rem[i];
-            uint32_t sign = (r >> 7) & 1u;
-            uint32_t m = r & 0x7Fu;
-            uint32_t bits = (sign << 15) | ((uint32_t)exps[i] << 7) | m;
-            wr_le(dst + 2 * i, bits, 2);
-        }
-        return ORC_OK;
+    const int width = 8 * es;
+    for (uint64_t i = 0; i < n; ++i) {
+        uint32_t r = get_rem(dtype, rem, i);
+        uint32_t sign = (r >> mbits) & 1u;
+        uint32_t m = r & ((1u << mbits) - 1u);
+        uint32_t bits = (sign << (width - 1)) | ((uint32_t)exps[i] << mbits) | m;
+        wr_le(dst + (uint64_t)es * i, bits, es);
     }
-    if (dtype == ORC_FP32) {
-        for (uint64_t i = 0; i < n; ++i) {
-            uint32_t r = (uint32_t)rd_le(rem + 3 * i, 3);
-            uint32_t sign = (r >> 23) & 1u;
-            uint32_t m = r & 0x7FFFFFu;
-            uint32_t bits = (sign << 31) | ((uint32_t)exps[i] << 23) | m;
-            wr_le(dst + 4 * i, bits, 4);
-        }
-        return ORC_OK;
-    }
-    return ORC_ERR_UNSUPPORTED_DTYPE;
+    return ORC_OK;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -373,9 +404,9 @@ int orc_decode_chunk(const uint8_t* stream, uint32_t len, int raw, uint32_t n_c,
 /*                  u64 exp_offset | u64 total_bytes | 16 zero bytes          */
 /*   [64,64+8C)     u64 offset of chunk c's stream from exp_offset            */
 /*   [64+8C,64+12C) u32 length of chunk c (bit 31 = RAW)                      */
-/*   rem_offset = round16(64+12C):      remainder plane, n*rb bytes           */
-/*   exp_offset = round16(rem_offset + n*rb): chunk streams, each padded to   */
-/*                16 bytes; every padding byte is zero.                       */
+/*   rem_offset = round16(64+12C):      remainder plane (R1, R21, R22)        */
+/*   exp_offset = round16(rem_offset + plane bytes): chunk streams, each      */
+/*                padded to 16 bytes; every padding byte is zero.             */
 
 static uint64_t num_chunks(uint64_t n) { return (n + ORC_CHUNK_ELEMS - 1) / ORC_CHUNK_ELEMS; }
 
@@ -388,7 +419,7 @@ static uint32_t chunk_elems(uint64_t n, uint64_t c) {
 static uint64_t rem_offset_of(uint64_t n) { return round16(ORC_HEADER_BYTES + 12u * num_chunks(n)); }
 
 static uint64_t exp_offset_of(int dtype, uint64_t n) {
-    return round16(rem_offset_of(n) + n * (uint64_t)remainder_bytes(dtype));
+    return round16(rem_offset_of(n) + orc_remainder_plane_bytes(dtype, n));
 }
 
 uint64_t orc_container_bound(int dtype, uint64_t n) {
@@ -400,7 +431,7 @@ uint64_t orc_container_bound(int dtype, uint64_t n) {
 
 int orc_compress(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t cap,
                  uint64_t* total) {
-    if (dtype != ORC_BF16 && dtype != ORC_FP32) return ORC_ERR_UNSUPPORTED_DTYPE;
+    if (!dtype_ok(dtype)) return ORC_ERR_UNSUPPORTED_DTYPE;
     if (num_chunks(n) > 0xFFFFFFFFull) return ORC_ERR_INVALID_ARG;
     if ((n > 0 && in == NULL) || out == NULL) return ORC_ERR_INVALID_ARG;
     uint64_t bound = orc_container_bound(dtype, n);
@@ -451,7 +482,7 @@ int orc_compress(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t c
 
 /* R12: the receiver checks the header and every chunk before trusting it. */
 int orc_decompress(const uint8_t* comp, uint64_t comp_bytes, int dtype, uint64_t n, void* out) {
-    if (dtype != ORC_BF16 && dtype != ORC_FP32) return ORC_ERR_UNSUPPORTED_DTYPE;
+    if (!dtype_ok(dtype)) return ORC_ERR_UNSUPPORTED_DTYPE;
     if (comp == NULL || (n > 0 && out == NULL)) return ORC_ERR_INVALID_ARG;
     if (comp_bytes < ORC_HEADER_BYTES) return ORC_ERR_CORRUPT;
     const uint8_t* h = comp;

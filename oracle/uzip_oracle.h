@@ -44,6 +44,9 @@ extern "C" {
 /* dtype codes, identical in value to the library's public enum */
 #define ORC_BF16 0
 #define ORC_FP32 1
+#define ORC_FP16 2
+#define ORC_FP8_E4M3 3
+#define ORC_FP8_E5M2 4
 
 /* status codes, identical in value to the library's public enum */
 #define ORC_OK 0
@@ -52,9 +55,14 @@ extern "C" {
 #define ORC_ERR_CAPACITY 3
 #define ORC_ERR_CORRUPT 4
 
-/* --- element split / merge (R1) ------------------------------------------ */
-/* Split n elements into exponent bytes (exps[n]) and remainder bytes
- * (rem[n*rb], rb = 1 for bf16, 3 for fp32, little endian). */
+/* --- element split / merge (R1, R21, R22) -------------------------------- */
+/* Bytes of the remainder plane of n elements: n (bf16), 3n (fp32, 3-byte
+ * little-endian fields), 2n (fp16, 2-byte fields), ceil(n/2) (both fp8
+ * formats: one 4-bit field per element, element 2j in the low nibble of byte
+ * j).  0 for an unknown dtype. */
+uint64_t orc_remainder_plane_bytes(int dtype, uint64_t n);
+/* Split n elements into exponent bytes (exps[n]) and the remainder plane
+ * (rem[orc_remainder_plane_bytes(dtype, n)]). */
 int orc_split(int dtype, const void* in, uint64_t n, uint8_t* exps, uint8_t* rem);
 /* Inverse of orc_split. */
 int orc_merge(int dtype, const uint8_t* exps, const uint8_t* rem, uint64_t n, void* out);

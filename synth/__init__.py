@@ -283,3 +283,61 @@ def uniform_pm1_bf16(n: int, cfg: int = 9, tensor: int = 0) -> np.ndarray:
         return f32_to_bf16_bits((2.0 * uniform(key, idx, 1, 0) - 1.0).astype(np.float32))
 
     return _parallel_fill(np.empty(n, np.uint16), n, fn)
+
+
+# --------------------------------------------------------------------------
+# fp16 and the two fp8 formats (the dtype sweep of UCCL-Zip Fig. 12): the
+# same N(0, std) stream, rounded to each element format
+
+def normal_fp16(n: int, std: float = 0.02, cfg: int = 10, tensor: int = 0, start: int = 0) -> np.ndarray:
+    """n fp16 ~ N(0, std) (numpy's round-to-nearest-even), as float16."""
+    key = stream_key(cfg, tensor)
+
+    def fn(lo, hi):
+        idx = np.arange(start + lo, start + hi, dtype=np.uint64)
+        return (normal(key, idx, 2, 0) * std).astype(np.float16).view(np.uint16)
+
+    return _parallel_fill(np.empty(n, np.uint16), n, fn).view(np.float16)
+
+
+FP8_FORMATS = {"e4m3": (4, 3, 7), "e5m2": (5, 2, 15)}  # exponent bits, fraction bits, bias
+
+
+def _fp8_positive_codes(fmt: str):
+    """Finite non-negative fp8 codes of a format, sorted by value."""
+    eb, mb, bias = FP8_FORMATS[fmt]
+    codes, vals = [], []
+    for c in range(128):
+        e, m = c >> mb, c & ((1 << mb) - 1)
+        if fmt == "e4m3" and e == 15 and m == (1 << mb) - 1:
+            continue  # NaN (e4m3fn has no infinities)
+        if fmt == "e5m2" and e == 31:
+            continue  # infinities and NaNs
+        v = (m / (1 << mb)) * 2.0 ** (1 - bias) if e == 0 else (1 + m / (1 << mb)) * 2.0 ** (e - bias)
+        codes.append(c)
+        vals.append(v)
+    order = np.argsort(vals, kind="stable")
+    return np.array(vals)[order], np.array(codes, np.uint8)[order]
+
+
+def round_to_fp8(x: np.ndarray, fmt: str) -> np.ndarray:
+    """Nearest finite fp8 code of each value (magnitudes beyond the largest
+    finite value saturate; ties go to the smaller magnitude), as uint8 bits."""
+    vals, codes = _fp8_positive_codes(fmt)
+    a = np.abs(x.astype(np.float64))
+    hi = np.clip(np.searchsorted(vals, a), 1, vals.size - 1)
+    lo = hi - 1
+    pick = np.where(a - vals[lo] <= vals[hi] - a, lo, hi)
+    pick = np.where(a >= vals[-1], vals.size - 1, pick)
+    return (codes[pick] | np.where(np.signbit(x), np.uint8(0x80), np.uint8(0))).astype(np.uint8)
+
+
+def normal_fp8(n: int, fmt: str, std: float = 0.02, cfg: int = 11, tensor: int = 0, start: int = 0) -> np.ndarray:
+    """n fp8 (fmt 'e4m3' or 'e5m2') ~ N(0, std), as uint8 bit patterns."""
+    key = stream_key(cfg, tensor)
+
+    def fn(lo, hi):
+        idx = np.arange(start + lo, start + hi, dtype=np.uint64)
+        return round_to_fp8(normal(key, idx, 2, 0) * std, fmt)
+
+    return _parallel_fill(np.empty(n, np.uint8), n, fn)
