@@ -1,5 +1,5 @@
 /*
- * uzip -- lossless compression of bf16 / fp32 GPU tensors (C ABI).
+ * uzip -- lossless compression of bf16 / fp16 / fp32 / fp8 GPU tensors (C ABI).
  *
  * What it computes.  Each value is split into its exponent field and the
  * remaining sign and fraction bits; only the exponent field is entropy coded
@@ -17,11 +17,18 @@
  *                   16 zero bytes
  *   [64, 64+8C)     u64 offset of chunk c's stream, relative to exp_offset
  *   [64+8C, 64+12C) u32 length of chunk c's stream, bit 31 = stored RAW
- *   rem_offset = round16(64 + 12C): remainder plane, n*rb bytes in element
- *                   order (bf16: rb = 1, sign<<7 | fraction; fp32: rb = 3,
- *                   sign<<23 | fraction, little endian)
- *   exp_offset = round16(rem_offset + n*rb): one stream per chunk, each
+ *   rem_offset = round16(64 + 12C): remainder plane in element order, the
+ *                   sign placed just above the fraction: bf16 1 byte
+ *                   (sign<<7 | fraction), fp16 2 bytes (sign<<10 |
+ *                   fraction), fp32 3 bytes (sign<<23 | fraction), fp8
+ *                   e4m3fn / e5m2 one 4-bit field (sign<<3 | fraction,
+ *                   sign<<2 | fraction) per element, two per byte, element
+ *                   2j in the low nibble of byte j; multi-byte fields are
+ *                   little endian.  P = its size in bytes.
+ *   exp_offset = round16(rem_offset + P): one stream per chunk, each
  *                   starting 16-byte aligned and zero padded to 16 bytes.
+ *   The exponent field (8 bits for bf16 and fp32, 5 for fp16 and e5m2, 4
+ *   for e4m3fn) is the symbol, one byte per element.
  *   A coded stream is u32 state[32], u8 bitmap[32] of present exponent
  *   bytes, u16 freq[K] (present bytes ascending, summing to 4096) and
  *   u16 words[W]: 32 interleaved rANS states (32-bit, 16-bit renormalisation,
@@ -50,7 +57,16 @@
 extern "C" {
 #endif
 
-typedef enum { UZIP_BF16 = 0, UZIP_FP32 = 1 } uzip_dtype;
+/* UZIP_FP16 is IEEE binary16; UZIP_FP8_E4M3 and UZIP_FP8_E5M2 are the OCP
+ * 8-bit formats float8_e4m3fn and float8_e5m2 (UCCL-Zip Fig. 12 runs its
+ * codec on all five). */
+typedef enum {
+    UZIP_BF16 = 0,
+    UZIP_FP32 = 1,
+    UZIP_FP16 = 2,
+    UZIP_FP8_E4M3 = 3,
+    UZIP_FP8_E5M2 = 4
+} uzip_dtype;
 
 typedef enum {
     UZIP_OK = 0,
@@ -119,9 +135,10 @@ uzip_status uzip_compress_ex(const void* d_in, uzip_dtype dtype, uint64_t n, voi
  *                    so the array is 131,088 bytes), else UZIP_ERR_TOO_LARGE.
  *   d_out            device, 16-byte aligned; out_capacity must be at least
  *                    the largest container (every chunk stored RAW):
- *                    round16(round16(64 + 12 C) + n * rb) + (C - 1) * 65536
+ *                    round16(round16(64 + 12 C) + P) + (C - 1) * 65536
  *                    + round16(n - (C - 1) * 65536) bytes for C > 0 chunks,
- *                    64 for n = 0, with rb = 1 (bf16) or 3 (fp32) (else
+ *                    64 for n = 0, with P the remainder plane's size (n,
+ *                    2n, 3n or ceil(n/2) bytes, see above) (else
  *                    UZIP_ERR_CAPACITY).
  *   d_out_size, d_status  as uzip_compress_ex (both nullable).
  * The result is byte for byte the container uzip_compress writes.  The call

@@ -15,7 +15,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "lib", "libuzip.so")
 
-UZIP_BF16, UZIP_FP32 = 0, 1
+UZIP_BF16, UZIP_FP32, UZIP_FP16, UZIP_FP8_E4M3, UZIP_FP8_E5M2 = 0, 1, 2, 3, 4
 UZIP_OK = 0
 UZIP_ERR_INVALID_ARG = 1
 UZIP_ERR_UNSUPPORTED_DTYPE = 2
@@ -129,13 +129,22 @@ def _check(st: int, what: str):
         raise UzipError(st, what)
 
 
-def dtype_code(t) -> int:
+def _torch_dtypes():
+    """uzip dtype code <-> torch dtype (the fp8 types where torch has them)."""
     import torch
 
-    if t.dtype == torch.bfloat16:
-        return UZIP_BF16
-    if t.dtype == torch.float32:
-        return UZIP_FP32
+    m = {UZIP_BF16: torch.bfloat16, UZIP_FP32: torch.float32, UZIP_FP16: torch.float16}
+    if hasattr(torch, "float8_e4m3fn"):
+        m[UZIP_FP8_E4M3] = torch.float8_e4m3fn
+    if hasattr(torch, "float8_e5m2"):
+        m[UZIP_FP8_E5M2] = torch.float8_e5m2
+    return m
+
+
+def dtype_code(t) -> int:
+    for code, tdt in _torch_dtypes().items():
+        if t.dtype == tdt:
+            return code
     raise UzipError(UZIP_ERR_UNSUPPORTED_DTYPE, f"dtype {t.dtype}")
 
 
@@ -146,7 +155,7 @@ def _stream(stream):
 
 
 def compress(t, stream=None, out=None, out_size=None):
-    """Compress a contiguous CUDA bf16/fp32 tensor.
+    """Compress a contiguous CUDA bf16, fp16, fp32 or fp8 tensor.
 
     Returns (buffer, size): buffer is a uint8 CUDA tensor of
     uzip_max_compressed_size bytes whose first `size` bytes (a 0-dim int64
@@ -181,10 +190,11 @@ def decompress(comp, dtype, n: int, stream=None, out=None, status=None, check: b
     """
     import torch
 
-    d = UZIP_BF16 if dtype in (torch.bfloat16, UZIP_BF16) else UZIP_FP32 if dtype in (torch.float32, UZIP_FP32) else -1
+    table = _torch_dtypes()
+    d = next((c for c, t in table.items() if dtype == c or dtype == t), -1)
     if d < 0:
         raise UzipError(UZIP_ERR_UNSUPPORTED_DTYPE, f"dtype {dtype}")
-    tdt = torch.bfloat16 if d == UZIP_BF16 else torch.float32
+    tdt = table[d]
     if out is None:
         out = torch.empty(n, dtype=tdt, device=comp.device)
     if status is None:

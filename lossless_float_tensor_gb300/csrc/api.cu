@@ -13,7 +13,6 @@ namespace {
 
 using namespace uzip;
 
-bool valid_dtype(int d) { return d == UZIP_BF16 || d == UZIP_FP32; }
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 typedef CUresult (*AddrRangeFn)(CUdeviceptr*, size_t*, CUdeviceptr);

@@ -39,18 +39,22 @@ struct CompressArgs {
 
 // element traits --------------------------------------------------------------
 template <int DT>
-struct Traits;
-template <>
-struct Traits<UZIP_BF16> {
-    static constexpr uint32_t kEs = 2;
-    __device__ static uint32_t exp_of(uint32_t b) { return (b >> 7) & 0xFFu; }
-    __device__ static uint32_t table_off(uint32_t b) { return (b >> 4) & 0x7F8u; }  // exponent * 8
-};
-template <>
-struct Traits<UZIP_FP32> {
-    static constexpr uint32_t kEs = 4;
-    __device__ static uint32_t exp_of(uint32_t b) { return (b >> 23) & 0xFFu; }
-    __device__ static uint32_t table_off(uint32_t b) { return (b >> 20) & 0x7F8u; }
+struct Traits {
+    static constexpr uint32_t kEs = Fmt<DT>::kEs;
+    static constexpr uint32_t kEmask = (1u << Fmt<DT>::kEbits) - 1u;
+    __device__ static uint32_t exp_of(uint32_t b) { return (b >> Fmt<DT>::kMbits) & kEmask; }
+    __device__ static uint32_t table_off(uint32_t b) { return exp_of(b) << 3; }  // exponent * 8
+    // sign|fraction field of one element (sign just above the fraction)
+    __device__ static uint32_t rem_of(uint32_t b) {
+        constexpr uint32_t mb = Fmt<DT>::kMbits, top = 8 * kEs - 1;
+        return ((b >> (top - mb)) & (1u << mb)) | (b & ((1u << mb) - 1u));
+    }
+    // load element i
+    __device__ static uint32_t load(const uint8_t* p, uint64_t i) {
+        if (kEs == 1) return p[i];
+        if (kEs == 2) return reinterpret_cast<const uint16_t*>(p)[i];
+        return reinterpret_cast<const uint32_t*>(p)[i];
+    }
 };
 
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
@@ -92,11 +96,16 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
     // A unit is 16 consecutive values (32 bytes of bf16, 64 of fp32) handled by
     // one lane: its remainder bytes (16 or 48) and exponent bytes (16) leave as
     // full 16-byte stores.
-    constexpr uint32_t PV = DT == UZIP_BF16 ? 2 : 4;  // 16-byte vectors per unit
+    static_assert(!Fmt<DT>::kPacked, "byte-field formats only");
+    constexpr uint32_t es = Fmt<DT>::kEs, mb = Fmt<DT>::kMbits;
+    constexpr uint32_t PV = es == 4 ? 4 : 2;  // 16-byte vectors per unit
     const uint32_t nunits = n_c / 16;
     auto process = [&](const uint4 (&q)[PV], uint32_t unit) {
         uint32_t ex[4];
-        if (DT == UZIP_BF16) {
+        if constexpr (es == 2) {
+            // two values per word; exponent field of both at bytes 0 and 2
+            constexpr uint32_t em2 = Traits<DT>::kEmask * 0x10001u;
+            constexpr uint32_t sgn = (1u << mb) * 0x10001u, frac = ((1u << mb) - 1u) * 0x10001u;
             uint32_t r[8];
 #pragma unroll
             for (int v = 0; v < 2; ++v) {
@@ -104,8 +113,8 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
                 uint32_t eb[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    r[4 * v + j] = ((w[j] >> 8) & 0x00800080u) | (w[j] & 0x007F007Fu);
-                    eb[j] = (w[j] >> 7) & 0x00FF00FFu;  // exponents of both values, bytes 0 and 2
+                    r[4 * v + j] = ((w[j] >> (15 - mb)) & sgn) | (w[j] & frac);
+                    eb[j] = (w[j] >> mb) & em2;
                     count((eb[j] << 6) & 0x3FC0u);
                     count((eb[j] >> 10) & 0x3FC0u);
                 }
@@ -148,7 +157,7 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
         for (int v = 0; v < int(PV); ++v) q[v] = ld_v4_hint(cin + (uint64_t(unit) * PV + v) * 16, pol_stream);
     };
     // Batches of U units per lane, two batches in flight.
-    constexpr int U = DT == UZIP_BF16 ? 4 : 2;
+    constexpr int U = es == 4 ? 2 : 4;
     const uint32_t nb = nunits / (32 * U);
     const uint32_t head = nunits - nb * 32 * U;
     for (uint32_t u = lane; u < head; u += 32) {
@@ -174,21 +183,136 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
     }
     // ragged tail (n_c not a multiple of 16): element by element
     for (uint32_t i = nunits * 16 + lane; i < n_c; i += 32) {
-        uint32_t e;
-        if (DT == UZIP_BF16) {
-            const uint32_t b = reinterpret_cast<const uint16_t*>(cin)[i];
-            rem_dst[i] = uint8_t(((b >> 8) & 0x80u) | (b & 0x7Fu));
-            e = (b >> 7) & 0xFFu;
-        } else {
-            const uint32_t b = reinterpret_cast<const uint32_t*>(cin)[i];
-            const uint32_t r = (b & 0x7FFFFFu) | ((b >> 8) & 0x800000u);
-            rem_dst[3 * uint64_t(i)] = uint8_t(r);
-            rem_dst[3 * uint64_t(i) + 1] = uint8_t(r >> 8);
-            rem_dst[3 * uint64_t(i) + 2] = uint8_t(r >> 16);
-            e = (b >> 23) & 0xFFu;
-        }
+        const uint32_t b = Traits<DT>::load(cin, i);
+        const uint32_t r = Traits<DT>::rem_of(b);
+        const uint32_t e = Traits<DT>::exp_of(b);
+#pragma unroll
+        for (uint32_t k = 0; k < es - 1; ++k) rem_dst[(es - 1) * uint64_t(i) + k] = uint8_t(r >> (8 * k));
         count(e << 6);
         if (ex_dst) ex_dst[i] = uint8_t(e);
+    }
+    __syncwarp();
+}
+
+// The same pass for formats whose sign|fraction field is not a whole number
+// of bytes (fp16: 11 bits, fp8 e4m3fn: 4, e5m2: 3): a unit is 32 values, whose
+// W-bit fields pack into exactly W 32-bit words, least significant bit first.
+template <int DT>
+__device__ void split_and_count_packed(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* __restrict__ rem_dst,
+                                       uint8_t* __restrict__ ex_dst, uint8_t* hist, uint32_t lane,
+                                       uint64_t pol_stream) {
+    static_assert(Fmt<DT>::kPacked, "packed-field formats only");
+    constexpr uint32_t es = Fmt<DT>::kEs, mb = Fmt<DT>::kMbits, W = Fmt<DT>::kRbits;
+    {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll 8
+        for (uint32_t i = lane; i < kRegionA / 16; i += 32) reinterpret_cast<uint4*>(hist)[i] = z;
+    }
+    __syncwarp();
+    uint8_t* hl = hist + 4 * (lane & 15);
+    auto count = [&](uint32_t e64) { atomicAdd(reinterpret_cast<uint32_t*>(hl + e64), 1u); };
+    constexpr uint32_t PV = 2 * es;  // 16-byte vectors per 32-value unit
+    const uint32_t nunits = n_c / 32;
+    auto process = [&](const uint4 (&q)[PV], uint32_t unit) {
+        uint32_t w[4 * PV];
+#pragma unroll
+        for (int v = 0; v < int(PV); ++v) w[4 * v] = q[v].x, w[4 * v + 1] = q[v].y, w[4 * v + 2] = q[v].z, w[4 * v + 3] = q[v].w;
+        uint32_t f[32];  // sign|fraction field of each value
+        uint32_t ex[8];  // exponent symbols, four per word
+        if constexpr (es == 2) {
+            constexpr uint32_t em2 = Traits<DT>::kEmask * 0x10001u;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const uint32_t eb = (w[j] >> mb) & em2;  // both exponents, bytes 0 and 2
+                count((eb << 6) & 0x3FC0u);
+                count((eb >> 10) & 0x3FC0u);
+                f[2 * j] = Traits<DT>::rem_of(w[j] & 0xFFFFu);
+                f[2 * j + 1] = Traits<DT>::rem_of(w[j] >> 16);
+                if (j & 1) ex[j >> 1] = __byte_perm((w[j - 1] >> mb) & em2, eb, 0x6420);
+            }
+        } else {
+            constexpr uint32_t em4 = Traits<DT>::kEmask * 0x01010101u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                ex[j] = (w[j] >> mb) & em4;
+                count((ex[j] << 6) & 0x3FC0u);
+                count((ex[j] >> 2) & 0x3FC0u);
+                count((ex[j] >> 10) & 0x3FC0u);
+                count((ex[j] >> 18) & 0x3FC0u);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) f[4 * j + k] = Traits<DT>::rem_of((w[j] >> (8 * k)) & 0xFFu);
+            }
+        }
+        uint32_t o[W];
+#pragma unroll
+        for (uint32_t k = 0; k < W; ++k) o[k] = 0;
+#pragma unroll
+        for (uint32_t k = 0; k < 32; ++k) {  // field k at bit W k
+            const uint32_t bit = W * k, wd = bit >> 5, sh = bit & 31;
+            o[wd] |= f[k] << sh;
+            if (sh + W > 32) o[wd + 1] |= f[k] >> (32 - sh);
+        }
+        uint32_t* rd = reinterpret_cast<uint32_t*>(rem_dst + uint64_t(unit) * 4 * W);
+#pragma unroll
+        for (uint32_t k = 0; k < W; ++k) st_u32_hint(rd + k, o[k], pol_stream);
+        if (ex_dst) {
+            reinterpret_cast<uint4*>(ex_dst + 32 * uint64_t(unit))[0] = make_uint4(ex[0], ex[1], ex[2], ex[3]);
+            reinterpret_cast<uint4*>(ex_dst + 32 * uint64_t(unit))[1] = make_uint4(ex[4], ex[5], ex[6], ex[7]);
+        }
+    };
+    auto load_unit = [&](uint4 (&q)[PV], uint32_t unit) {
+#pragma unroll
+        for (int v = 0; v < int(PV); ++v) q[v] = ld_v4_hint(cin + (uint64_t(unit) * PV + v) * 16, pol_stream);
+    };
+    // batches of U units per lane, two batches in flight
+    constexpr int U = es == 2 ? 2 : 4;
+    const uint32_t nb = nunits / (32 * U);
+    const uint32_t head = nunits - nb * 32 * U;
+    for (uint32_t u = lane; u < head; u += 32) {
+        uint4 q[PV];
+        load_unit(q, u);
+        process(q, u);
+    }
+    uint4 qa[U][PV], qb[U][PV];
+    auto unit_of = [&](uint32_t k, int u) -> uint32_t { return head + k * 32 * U + 32 * u + lane; };
+    auto load = [&](uint4 (&q)[U][PV], uint32_t k) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) load_unit(q[u], unit_of(k, u));
+    };
+    if (nb > 0) load(qa, 0);
+    for (uint32_t k = 0; k < nb; k += 2) {
+        if (k + 1 < nb) load(qb, k + 1);
+#pragma unroll
+        for (int u = 0; u < U; ++u) process(qa[u], unit_of(k, u));
+        if (k + 1 >= nb) break;
+        if (k + 2 < nb) load(qa, k + 2);
+#pragma unroll
+        for (int u = 0; u < U; ++u) process(qb[u], unit_of(k + 1, u));
+    }
+    // ragged tail (fewer than 32 values): its fields start byte aligned
+    // (32 W bits per unit); lane 0 packs them, the lanes count and copy the
+    // exponents
+    const uint32_t i0 = nunits * 32;
+    if (i0 < n_c) {
+        if (lane == 0) {
+            uint64_t acc = 0;
+            uint32_t nacc = 0, out = i0 / 8 * W;
+            for (uint32_t i = i0; i < n_c; ++i) {
+                acc |= uint64_t(Traits<DT>::rem_of(Traits<DT>::load(cin, i))) << nacc;
+                nacc += W;
+                while (nacc >= 8) {
+                    rem_dst[out++] = uint8_t(acc);
+                    acc >>= 8;
+                    nacc -= 8;
+                }
+            }
+            if (nacc) rem_dst[out] = uint8_t(acc);
+        }
+        for (uint32_t i = i0 + lane; i < n_c; i += 32) {
+            const uint32_t e = Traits<DT>::exp_of(Traits<DT>::load(cin, i));
+            count(e << 6);
+            if (ex_dst) ex_dst[i] = uint8_t(e);
+        }
     }
     __syncwarp();
 }
@@ -401,7 +525,7 @@ __device__ __forceinline__ void load_block(uint32_t (&v)[32], const uint8_t* cin
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         const uint8_t* p = cin + es * (uint64_t(uint32_t(t - j)) * 32 + lane);
-        v[j] = es == 2 ? ld_u16_hint(p, pol) : ld_u32_hint(p, pol);
+        v[j] = es == 1 ? uint32_t(*p) : es == 2 ? ld_u16_hint(p, pol) : ld_u32_hint(p, pol);
     }
 }
 
@@ -439,7 +563,10 @@ __device__ bool encode_chunk(const uint8_t* __restrict__ cin, uint32_t n_c, uint
         const uint32_t i = 32 * uint32_t(t) + lane;
         const bool active = i < n_c;
         uint32_t bits = 0;
-        if (active) bits = es == 2 ? ld_u16_hint(cin + 2 * uint64_t(i), pol) : ld_u32_hint(cin + 4 * uint64_t(i), pol);
+        if (active)
+            bits = es == 1   ? uint32_t(cin[i])
+                   : es == 2 ? ld_u16_hint(cin + 2 * uint64_t(i), pol)
+                             : ld_u32_hint(cin + 4 * uint64_t(i), pol);
         enc_step<DT, S>(st, bits, active, table_s, gwords, lt);
         if (S == Sink::Count && hdr_bytes + 2u * uint32_t(-st.pos) >= n_c) return false;
     }
@@ -615,18 +742,23 @@ __device__ void discard_slot(uint8_t* slot, uint32_t first_byte, uint32_t last_b
 // RAW chunk: the n_c exponent bytes, zero padded to 16
 template <int DT>
 __device__ void write_raw(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* dst, uint32_t lane) {
+    constexpr uint32_t es = Fmt<DT>::kEs, mb = Fmt<DT>::kMbits;
     const uint32_t nb = (n_c + 15) / 16;
     for (uint32_t b = lane; b < nb; b += 32) {
         const uint32_t i0 = 16 * b;
         uint32_t o[4] = {0, 0, 0, 0};
         if (i0 + 16 <= n_c) {
-            if (DT == UZIP_BF16) {
+            if (es == 2) {
+                constexpr uint32_t em2 = Traits<DT>::kEmask * 0x10001u;
                 const uint4 q0 = *reinterpret_cast<const uint4*>(cin + 2 * uint64_t(i0));
                 const uint4 q1 = *reinterpret_cast<const uint4*>(cin + 2 * uint64_t(i0) + 16);
                 const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    o[j] = __byte_perm((w[2 * j] >> 7) & 0x00FF00FFu, (w[2 * j + 1] >> 7) & 0x00FF00FFu, 0x6420);
+                for (int j = 0; j < 4; ++j) o[j] = __byte_perm((w[2 * j] >> mb) & em2, (w[2 * j + 1] >> mb) & em2, 0x6420);
+            } else if (es == 1) {
+                constexpr uint32_t em4 = Traits<DT>::kEmask * 0x01010101u;
+                const uint4 q = *reinterpret_cast<const uint4*>(cin + uint64_t(i0));
+                o[0] = (q.x >> mb) & em4, o[1] = (q.y >> mb) & em4, o[2] = (q.z >> mb) & em4, o[3] = (q.w >> mb) & em4;
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -636,11 +768,8 @@ __device__ void write_raw(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t
                 }
             }
         } else {
-            for (uint32_t k = 0; k < 16 && i0 + k < n_c; ++k) {
-                const uint32_t bits = DT == UZIP_BF16 ? reinterpret_cast<const uint16_t*>(cin)[i0 + k]
-                                                      : reinterpret_cast<const uint32_t*>(cin)[i0 + k];
-                o[k >> 2] |= Traits<DT>::exp_of(bits) << (8 * (k & 3));
-            }
+            for (uint32_t k = 0; k < 16 && i0 + k < n_c; ++k)
+                o[k >> 2] |= Traits<DT>::exp_of(Traits<DT>::load(cin, i0 + k)) << (8 * (k & 3));
         }
         *reinterpret_cast<uint4*>(dst + 16 * uint64_t(b)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -778,7 +907,6 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
     const uint64_t rem_off = rem_offset(n);
     const uint64_t exp_off = exp_offset(DT, n);
     constexpr uint32_t es = Traits<DT>::kEs;
-    constexpr uint32_t rb = DT == UZIP_BF16 ? 1 : 3;
     const uint64_t pol_keep = policy_evict_last();
     const uint64_t pol_stream = policy_evict_first();
     const uint32_t processed = C - a.first_ticket;
@@ -823,7 +951,7 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
             *reinterpret_cast<uint64_t*>(h + 48) = 0;
             *reinterpret_cast<uint64_t*>(h + 56) = 0;
             for (uint64_t i = kHeader + 12 * uint64_t(C); i < rem_off; ++i) h[i] = 0;
-            for (uint64_t i = rem_off + n * rb; i < exp_off; ++i) h[i] = 0;
+            for (uint64_t i = rem_off + rem_plane_bytes(DT, n); i < exp_off; ++i) h[i] = 0;
             if (a.out_size) *a.out_size = total;
             if (a.status_out) *a.status_out = int32_t(st ? st : (total ? 0u : uint32_t(UZIP_ERR_TIMEOUT)));
         }
@@ -859,8 +987,12 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
         uint8_t* slot = slots ? slots + which * kSlotBytes : nullptr;
 
         // 1. plane split + exponent bytes + histogram
-        split_and_count<DT>(cin, n_c, a.out + rem_off + uint64_t(c) * kChunk * rb, slot, regA, lane, pol_keep,
-                            pol_stream);
+        if constexpr (Fmt<DT>::kPacked)
+            split_and_count_packed<DT>(cin, n_c, a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk, slot, regA, lane,
+                                       pol_stream);
+        else
+            split_and_count<DT>(cin, n_c, a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk, slot, regA, lane,
+                                pol_keep, pol_stream);
         uint32_t cnt[8];
         reduce_hist(regA, lane, cnt);
         __syncwarp();
@@ -970,7 +1102,11 @@ cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n
     a.num_chunks = uint32_t(C);
     a.stash = static_cast<uint8_t*>(stash);
 
-    void (*kern)(CompressArgs) = dtype == UZIP_BF16 ? compress_kernel<UZIP_BF16> : compress_kernel<UZIP_FP32>;
+    void (*kern)(CompressArgs) = dtype == UZIP_BF16       ? compress_kernel<UZIP_BF16>
+                                 : dtype == UZIP_FP32     ? compress_kernel<UZIP_FP32>
+                                 : dtype == UZIP_FP16     ? compress_kernel<UZIP_FP16>
+                                 : dtype == UZIP_FP8_E4M3 ? compress_kernel<UZIP_FP8_E4M3>
+                                                          : compress_kernel<UZIP_FP8_E5M2>;
     int sms = 0, per_sm = 0;
     if ((err = launch_shape(reinterpret_cast<const void*>(kern), 32, kCompressSmem, &sms, &per_sm)) != cudaSuccess)
         return err;

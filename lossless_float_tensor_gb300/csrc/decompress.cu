@@ -32,25 +32,49 @@ __device__ __forceinline__ uint32_t warp_excl_scan_d(uint32_t v, uint32_t lane, 
     return inc - v;
 }
 
+// element bits from exponent field e and sign|fraction field r
 template <int DT>
 __device__ __forceinline__ uint32_t merge_bits(uint32_t e, uint32_t r) {
-    if (DT == UZIP_BF16) return ((r & 0x80u) << 8) | (e << 7) | (r & 0x7Fu);
-    return ((r & 0x800000u) << 8) | (e << 23) | (r & 0x7FFFFFu);
+    constexpr uint32_t mb = Fmt<DT>::kMbits, top = 8 * Fmt<DT>::kEs - 1;
+    return ((r >> mb) << top) | (e << mb) | (r & ((1u << mb) - 1u));
 }
-// The same merge for the decode loop, with fewer logic-unit instructions:
-// r * 257 puts the remainder byte at bits 0..7 and again at 8..15, so one
-// mask keeps the fraction (bits 0..6) and the sign (bit 15).
+// The same merge for the decode loop, with fewer logic-unit instructions: for
+// bf16, r * 257 puts the remainder byte at bits 0..7 and again at 8..15, so
+// one mask keeps the fraction (bits 0..6) and the sign (bit 15).
 template <int DT>
 __device__ __forceinline__ uint32_t merge_fast(uint32_t e, uint32_t r) {
     if (DT == UZIP_BF16) return ((r * 257u) & 0x807Fu) | (e << 7);
-    return ((r & 0x7FFFFFu) | (e << 23)) | ((r << 8) & 0x80000000u);
+    if (DT == UZIP_FP32) return ((r & 0x7FFFFFu) | (e << 23)) | ((r << 8) & 0x80000000u);
+    return merge_bits<DT>(e, r);
+}
+// sign|fraction field of element i of a chunk's remainder plane (W-bit
+// fields packed least significant bit first; only the bytes holding the
+// field are read)
+template <int DT>
+__device__ __forceinline__ uint32_t rem_field(const uint8_t* __restrict__ rem, uint32_t i) {
+    if constexpr (DT == UZIP_BF16) return __ldg(rem + i);
+    if constexpr (DT == UZIP_FP32)
+        return uint32_t(__ldg(rem + 3 * i)) | uint32_t(__ldg(rem + 3 * i + 1)) << 8 | uint32_t(__ldg(rem + 3 * i + 2)) << 16;
+    constexpr uint32_t W = Fmt<DT>::kRbits;
+    const uint32_t bit = W * i, b0 = bit >> 3, sh = bit & 7;
+    uint32_t v = __ldg(rem + b0);
+    if (sh + W > 8) v |= uint32_t(__ldg(rem + b0 + 1)) << 8;
+    if (sh + W > 16) v |= uint32_t(__ldg(rem + b0 + 2)) << 16;
+    return (v >> sh) & ((1u << W) - 1u);
 }
 
 template <int DT>
 __device__ void merge_raw(const uint8_t* __restrict__ ex, const uint8_t* __restrict__ rem, uint8_t* __restrict__ out,
                           uint32_t n_c, uint32_t lane) {
-    constexpr uint32_t rb = DT == UZIP_BF16 ? 1 : 3;
-    constexpr uint32_t es = DT == UZIP_BF16 ? 2 : 4;
+    constexpr uint32_t es = Fmt<DT>::kEs;
+    if constexpr (DT != UZIP_BF16 && DT != UZIP_FP32) {  // element by element
+        for (uint32_t i = lane; i < n_c; i += 32) {
+            const uint32_t v = merge_bits<DT>(ex[i], rem_field<DT>(rem, i));
+            if (es == 2) reinterpret_cast<uint16_t*>(out)[i] = uint16_t(v);
+            else out[i] = uint8_t(v);
+        }
+        return;
+    }
     const uint32_t nfull = n_c / 16;
     for (uint32_t b = lane; b < nfull; b += 32) {
         const uint4 eq = *reinterpret_cast<const uint4*>(ex + 16 * uint64_t(b));
@@ -92,9 +116,7 @@ __device__ void merge_raw(const uint8_t* __restrict__ ex, const uint8_t* __restr
         }
     }
     for (uint32_t i = nfull * 16 + lane; i < n_c; i += 32) {
-        uint32_t r = rem[rb * uint64_t(i)];
-        if (DT == UZIP_FP32) r |= uint32_t(rem[3 * uint64_t(i) + 1]) << 8 | uint32_t(rem[3 * uint64_t(i) + 2]) << 16;
-        const uint32_t v = merge_bits<DT>(ex[i], r);
+        const uint32_t v = merge_bits<DT>(ex[i], rem_field<DT>(rem, i));
         if (es == 2) reinterpret_cast<uint16_t*>(out)[i] = uint16_t(v);
         else reinterpret_cast<uint32_t*>(out)[i] = v;
     }
@@ -107,7 +129,7 @@ __device__ void merge_raw(const uint8_t* __restrict__ ex, const uint8_t* __restr
 template <int DT, bool RING>
 __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, const uint8_t* __restrict__ rem,
                              uint8_t* __restrict__ out, uint32_t n_c, uint32_t lane, uint8_t* wsm) {
-    constexpr uint32_t es = DT == UZIP_BF16 ? 2 : 4;
+    constexpr uint32_t es = Fmt<DT>::kEs;
     uint8_t* slot_sym = wsm;                                                   // u8[4096]
     uint2* sym_gc = reinterpret_cast<uint2*>(wsm + kDecSlotTable);                  // {f - 4096, -cum}
     uint32_t* plist = reinterpret_cast<uint32_t*>(wsm + kDecSlotTable + kDecSymTable); // u32[256]: cum << 8 | s
@@ -219,17 +241,28 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
             const uint32_t v = merge_fast<DT>(s, r);
             const uint64_t i = 32 * uint64_t(t) + lane;
             if (es == 2) reinterpret_cast<uint16_t*>(out)[i] = uint16_t(v);
-            else reinterpret_cast<uint32_t*>(out)[i] = v;
+            else if (es == 4) reinterpret_cast<uint32_t*>(out)[i] = v;
+            else out[i] = uint8_t(v);
         }
     };
     auto gwin = [&]() -> uint32_t {
         const uint32_t widx = pos + lane;
         return __ldg(words + (widx < wlast ? widx : wlast));
     };
+    // Packed formats: a step's 32 fields are W consecutive words; this lane's
+    // field starts at bit W lane of them and may run into the next word.
+    constexpr uint32_t RB = Fmt<DT>::kRbits;
+    const uint32_t lword = (RB * lane) >> 5, lsh = (RB * lane) & 31;
+    const bool lstraddle = lsh + RB > 32;
     auto load_rem_full = [&](uint32_t t) -> uint32_t {  // t < 2048 of a full chunk
-        const uint32_t i = 32 * t + lane;
-        if (DT == UZIP_BF16) return __ldg(rem + i);
-        return uint32_t(__ldg(rem + 3 * i)) | uint32_t(__ldg(rem + 3 * i + 1)) << 8 | uint32_t(__ldg(rem + 3 * i + 2)) << 16;
+        if constexpr (!Fmt<DT>::kPacked) {
+            return rem_field<DT>(rem, 32 * t + lane);
+        } else {
+            const uint32_t* p = reinterpret_cast<const uint32_t*>(rem) + RB * t + lword;
+            const uint32_t lo = __ldg(p);
+            const uint32_t hi = lstraddle ? __ldg(p + 1) : 0u;
+            return __funnelshift_r(lo, hi, lsh) & ((1u << RB) - 1u);
+        }
     };
     auto load_rem = [&](uint32_t t) -> uint32_t {
         const uint32_t i = 32 * t + lane;
@@ -294,11 +327,11 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
         // Both streams are cold in L2 when decompression starts: pull the
         // remainder bytes of the steps 64 ahead and the stream bytes ~1 KiB
         // past the read position into L2 (one instruction each per 16 steps).
-        constexpr uint32_t rb = DT == UZIP_BF16 ? 1 : 3;
-        constexpr uint32_t kRemLines = 16 * 32 * rb / 128;
+        constexpr uint32_t kRemStep = Fmt<DT>::kRemChunk / kSteps;  // remainder bytes per step
+        constexpr uint32_t kRemLines = 16 * kRemStep / 128;
         auto prefetch_l2 = [&](uint32_t t_ahead) {
             if (lane < kRemLines && t_ahead + 16 <= kSteps)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(rem + uint64_t(t_ahead) * 32 * rb + 128 * lane));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(rem + uint64_t(t_ahead) * kRemStep + 128 * lane));
             if (lane >= 30) {
                 const uint32_t at = (rq - 2 * lane) + 1024 + 128 * (lane - 30);
                 if (at < nlines * 16) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + at));
@@ -372,8 +405,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 28 / kDecWarps) decompress_ker
     const uint32_t lane = threadIdx.x & 31;
     const uint32_t wid = threadIdx.x >> 5;
     uint8_t* wsm = smem + wid * kDecWarpSmem;
-    constexpr uint32_t es = DT == UZIP_BF16 ? 2 : 4;
-    constexpr uint32_t rb = DT == UZIP_BF16 ? 1 : 3;
+    constexpr uint32_t es = Fmt<DT>::kEs;
     const uint8_t* h = a.comp;
     const uint64_t n = a.n;
     const uint64_t C = num_chunks(n);
@@ -402,7 +434,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 28 / kDecWarps) decompress_ker
         bool good = (off & 15u) == 0 && off <= section && len <= section - off;
         if (good) {
             const uint8_t* src = h + exp_off + off;
-            const uint8_t* rem = h + rem_off + c * kChunk * rb;
+            const uint8_t* rem = h + rem_off + c * Fmt<DT>::kRemChunk;
             uint8_t* out = a.out + c * kChunk * es;
             if (raw) {
                 if (len == n_c) merge_raw<DT>(src, rem, out, n_c, lane);
@@ -426,7 +458,11 @@ cudaError_t launch_decompress(int dtype, const void* d_comp, uint64_t cap, void*
     if (d_status && (err = cudaMemsetAsync(d_status, 0, sizeof(int32_t), s)) != cudaSuccess) return err;
     DecompressArgs a{static_cast<const uint8_t*>(d_comp), cap, static_cast<uint8_t*>(d_out), n, d_status};
     const uint64_t C = num_chunks(n);  // C == 0 still launches one block to validate the header
-    void (*kern)(DecompressArgs) = dtype == UZIP_BF16 ? decompress_kernel<UZIP_BF16> : decompress_kernel<UZIP_FP32>;
+    void (*kern)(DecompressArgs) = dtype == UZIP_BF16       ? decompress_kernel<UZIP_BF16>
+                                   : dtype == UZIP_FP32     ? decompress_kernel<UZIP_FP32>
+                                   : dtype == UZIP_FP16     ? decompress_kernel<UZIP_FP16>
+                                   : dtype == UZIP_FP8_E4M3 ? decompress_kernel<UZIP_FP8_E4M3>
+                                                            : decompress_kernel<UZIP_FP8_E5M2>;
     const uint32_t smem = kDecWarps * kDecWarpSmem;
     int sms = 0, per_sm = 0;
     if ((err = launch_shape(reinterpret_cast<const void*>(kern), kDecWarps * 32, smem, &sms, &per_sm)) != cudaSuccess)

@@ -49,7 +49,7 @@ extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d
                                           void* const* h_bank, uint64_t h_capacity, uint64_t* h_sizes,
                                           uzip_pipe_mode mode, cudaStream_t s_compress, cudaStream_t s_copy) {
     using namespace uzip;
-    if (dtype != UZIP_BF16 && dtype != UZIP_FP32) return UZIP_ERR_UNSUPPORTED_DTYPE;
+    if (!valid_dtype(dtype)) return UZIP_ERR_UNSUPPORTED_DTYPE;
     if (n_msgs == 0 || !d_msgs || !msg_elems || !d_bank || !h_bank || !h_sizes) return UZIP_ERR_INVALID_ARG;
     if (mode != UZIP_PIPE_EXACT && mode != UZIP_PIPE_BOUND && mode != UZIP_PIPE_SERIAL && mode != UZIP_PIPE_SIZED)
         return UZIP_ERR_INVALID_ARG;

@@ -22,13 +22,52 @@ constexpr uint32_t kRawFlag = 0x80000000u;
 constexpr uint32_t kStreamHead = 160;     // 32 states + 32-byte bitmap
 
 __host__ __device__ inline uint64_t round16(uint64_t v) { return (v + 15) & ~uint64_t(15); }
-__host__ __device__ inline uint32_t rem_bytes(int dtype) { return dtype == UZIP_BF16 ? 1u : 3u; }
-__host__ __device__ inline uint32_t elem_bytes(int dtype) { return dtype == UZIP_BF16 ? 2u : 4u; }
+__host__ __device__ inline bool valid_dtype(int d) { return d >= UZIP_BF16 && d <= UZIP_FP8_E5M2; }
+__host__ __device__ inline uint32_t elem_bytes(int dtype) {
+    return dtype == UZIP_FP32 ? 4u : (dtype == UZIP_BF16 || dtype == UZIP_FP16) ? 2u : 1u;
+}
+// width of an element's sign|fraction field: 8 (bf16), 24 (fp32), 11 (fp16),
+// 4 (fp8 e4m3fn), 3 (fp8 e5m2)
+__host__ __device__ inline uint32_t rem_bits(int dtype) {
+    switch (dtype) {
+        case UZIP_BF16: return 8;
+        case UZIP_FP32: return 24;
+        case UZIP_FP16: return 11;
+        case UZIP_FP8_E4M3: return 4;
+        default: return 3;
+    }
+}
+// remainder plane bytes of n elements: the fields packed least significant
+// bit first
+__host__ __device__ inline uint64_t rem_plane_bytes(int dtype, uint64_t n) { return (n * rem_bits(dtype) + 7) / 8; }
 __host__ __device__ inline uint64_t num_chunks(uint64_t n) { return (n + kChunk - 1) / kChunk; }
 __host__ __device__ inline uint64_t rem_offset(uint64_t n) { return round16(kHeader + 12 * num_chunks(n)); }
 __host__ __device__ inline uint64_t exp_offset(int dtype, uint64_t n) {
-    return round16(rem_offset(n) + n * rem_bytes(dtype));
+    return round16(rem_offset(n) + rem_plane_bytes(dtype, n));
 }
+
+// Element format: bytes per element, exponent and fraction bit widths, the
+// remainder field width (sign + fraction) and a full chunk's share of the
+// remainder plane in bytes.
+template <int DT>
+struct Fmt;
+template <int ES, int EB, int MB>
+struct FmtOf {
+    static constexpr uint32_t kEs = ES, kEbits = EB, kMbits = MB, kRbits = MB + 1;
+    static constexpr uint32_t kRemChunk = kChunk / 8 * kRbits;
+    // formats whose fields are not whole bytes: packed 32 elements at a time
+    static constexpr bool kPacked = (kRbits % 8) != 0;
+};
+template <>
+struct Fmt<UZIP_BF16> : FmtOf<2, 8, 7> {};
+template <>
+struct Fmt<UZIP_FP32> : FmtOf<4, 8, 23> {};
+template <>
+struct Fmt<UZIP_FP16> : FmtOf<2, 5, 10> {};
+template <>
+struct Fmt<UZIP_FP8_E4M3> : FmtOf<1, 4, 3> {};
+template <>
+struct Fmt<UZIP_FP8_E5M2> : FmtOf<1, 5, 2> {};
 // Largest container: every chunk stored RAW (round16 of each chunk length).
 __host__ __device__ inline uint64_t container_bound(int dtype, uint64_t n) {
     uint64_t c = num_chunks(n);

@@ -46,14 +46,16 @@ static uint64_t round16(uint64_t v) { return (v + 15u) / 16u * 16u; }
 /* ------------------------------------------------------------------------ */
 /* R1, R21, R22: split each value into its exponent field and its           */
 /* sign|fraction bits, the sign placed just above the fraction.             */
-/* bf16    = s | e(8) | m(7):  rem = s<<7 | m    (1 byte)                   */
-/* fp32    = s | e(8) | m(23): rem = s<<23 | m   (3 bytes, LE)              */
-/* fp16    = s | e(5) | m(10): rem = s<<10 | m   (2 bytes, LE)              */
-/* e4m3fn  = s | e(4) | m(3):  rem = s<<3 | m    (4 bits)                   */
-/* e5m2    = s | e(5) | m(2):  rem = s<<2 | m    (4 bits, top bit 0)        */
-/* The 4-bit fields of the fp8 formats are packed two per byte: element 2j */
-/* in the low nibble of byte j, element 2j+1 in the high nibble (a missing */
-/* last element leaves it zero).                                            */
+/* bf16    = s | e(8) | m(7):  rem = s<<7 | m    (8-bit field)              */
+/* fp32    = s | e(8) | m(23): rem = s<<23 | m   (24-bit field)             */
+/* fp16    = s | e(5) | m(10): rem = s<<10 | m   (11-bit field)             */
+/* e4m3fn  = s | e(4) | m(3):  rem = s<<3 | m    (4-bit field)              */
+/* e5m2    = s | e(5) | m(2):  rem = s<<2 | m    (3-bit field)              */
+/* The remainder plane packs the w-bit fields back to back, least          */
+/* significant bit first: element i occupies bits [w*i, w*i + w) of the    */
+/* plane, bit k of the plane being bit k%8 of byte k/8.  For bf16 and fp32 */
+/* this is one byte / three little-endian bytes per element; bits past the */
+/* last field are zero.                                                     */
 
 /* (exponent bits, fraction bits, element bytes) of each dtype */
 static int layout(int dtype, int* ebits, int* mbits, int* es) {
@@ -72,34 +74,34 @@ static int dtype_ok(int dtype) {
     return layout(dtype, &eb, &mb, &es);
 }
 
+/* width of the remainder field: the sign bit and the fraction bits */
+static int field_bits(int dtype) {
+    int ebits, mbits, es;
+    return layout(dtype, &ebits, &mbits, &es) ? 1 + mbits : 0;
+}
+
 uint64_t orc_remainder_plane_bytes(int dtype, uint64_t n) {
-    switch (dtype) {
-        case ORC_BF16: return n;
-        case ORC_FP32: return 3 * n;
-        case ORC_FP16: return 2 * n;
-        case ORC_FP8_E4M3:
-        case ORC_FP8_E5M2: return (n + 1) / 2;
-        default: return 0;
-    }
+    return (n * (uint64_t)field_bits(dtype) + 7) / 8;
 }
 
-/* remainder field of element i: read / write */
+/* remainder field of element i: read / write, bit by bit */
 static uint32_t get_rem(int dtype, const uint8_t* rem, uint64_t i) {
-    if (dtype == ORC_FP8_E4M3 || dtype == ORC_FP8_E5M2) return (rem[i / 2] >> (4 * (i % 2))) & 0xFu;
-    if (dtype == ORC_BF16) return rem[i];
-    if (dtype == ORC_FP16) return (uint32_t)rd_le(rem + 2 * i, 2);
-    return (uint32_t)rd_le(rem + 3 * i, 3);
+    int w = field_bits(dtype);
+    uint32_t r = 0;
+    for (int k = 0; k < w; ++k) {
+        uint64_t bit = (uint64_t)w * i + (uint64_t)k;
+        r |= (uint32_t)((rem[bit / 8] >> (bit % 8)) & 1u) << k;
+    }
+    return r;
 }
 
+/* the plane must be zeroed first: fields are ORed in */
 static void put_rem(int dtype, uint8_t* rem, uint64_t i, uint32_t r) {
-    if (dtype == ORC_FP8_E4M3 || dtype == ORC_FP8_E5M2) {
-        if (i % 2 == 0) rem[i / 2] = (uint8_t)r; /* also clears the high nibble */
-        else rem[i / 2] = (uint8_t)(rem[i / 2] | (r << 4));
-        return;
+    int w = field_bits(dtype);
+    for (int k = 0; k < w; ++k) {
+        uint64_t bit = (uint64_t)w * i + (uint64_t)k;
+        rem[bit / 8] = (uint8_t)(rem[bit / 8] | (((r >> k) & 1u) << (bit % 8)));
     }
-    if (dtype == ORC_BF16) rem[i] = (uint8_t)r;
-    else if (dtype == ORC_FP16) wr_le(rem + 2 * i, r, 2);
-    else wr_le(rem + 3 * i, r, 3);
 }
 
 int orc_split(int dtype, const void* in, uint64_t n, uint8_t* exps, uint8_t* rem) {
@@ -107,6 +109,7 @@ int orc_split(int dtype, const void* in, uint64_t n, uint8_t* exps, uint8_t* rem
     if (!layout(dtype, &ebits, &mbits, &es)) return ORC_ERR_UNSUPPORTED_DTYPE;
     const uint8_t* src = (const uint8_t*)in;
     const int width = 8 * es;
+    memset(rem, 0, (size_t)orc_remainder_plane_bytes(dtype, n));
     for (uint64_t i = 0; i < n; ++i) {
         uint32_t bits = (uint32_t)rd_le(src + (uint64_t)es * i, es);
         uint32_t sign = (bits >> (width - 1)) & 1u;

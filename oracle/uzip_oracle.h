@@ -56,10 +56,10 @@ extern "C" {
 #define ORC_ERR_CORRUPT 4
 
 /* --- element split / merge (R1, R21, R22) -------------------------------- */
-/* Bytes of the remainder plane of n elements: n (bf16), 3n (fp32, 3-byte
- * little-endian fields), 2n (fp16, 2-byte fields), ceil(n/2) (both fp8
- * formats: one 4-bit field per element, element 2j in the low nibble of byte
- * j).  0 for an unknown dtype. */
+/* Bytes of the remainder plane of n elements: the sign|fraction fields of
+ * w = 1 + fraction bits each (8 bf16, 24 fp32, 11 fp16, 4 e4m3fn, 3 e5m2),
+ * packed least significant bit first, ceil(n*w/8) bytes.  0 for an unknown
+ * dtype. */
 uint64_t orc_remainder_plane_bytes(int dtype, uint64_t n);
 /* Split n elements into exponent bytes (exps[n]) and the remainder plane
  * (rem[orc_remainder_plane_bytes(dtype, n)]). */

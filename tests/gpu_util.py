@@ -1,11 +1,21 @@
 """Helpers for GPU tests: move bit patterns to the device and call the C ABI."""
 import numpy as np
 
-BF16, FP32 = 0, 1
+BF16, FP32, FP16, FP8_E4M3, FP8_E5M2 = 0, 1, 2, 3, 4
+ELEM_BYTES = {BF16: 2, FP32: 4, FP16: 2, FP8_E4M3: 1, FP8_E5M2: 1}
+BITS = {BF16: np.uint16, FP32: np.uint32, FP16: np.uint16, FP8_E4M3: np.uint8, FP8_E5M2: np.uint8}
 
 
 def dtype_of(bits):
-    return BF16 if bits.dtype == np.uint16 else FP32
+    """bf16 as uint16 bit patterns, fp16 as float16, fp32 as uint32/float32;
+    fp8 arrays (uint8) need the dtype given explicitly."""
+    if bits.dtype == np.uint16:
+        return BF16
+    if bits.dtype == np.float16:
+        return FP16
+    if bits.dtype in (np.uint32, np.float32):
+        return FP32
+    raise TypeError(f"pass the dtype for numpy {bits.dtype}")
 
 
 def to_device(bits):
@@ -13,6 +23,10 @@ def to_device(bits):
 
     if bits.dtype == np.uint16:
         return torch.from_numpy(bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    if bits.dtype == np.float16:
+        return torch.from_numpy(bits.copy()).cuda()
+    if bits.dtype == np.uint8:
+        return torch.from_numpy(bits.copy()).cuda()
     return torch.from_numpy(bits.view(np.int32).copy()).cuda().view(torch.float32)
 
 
@@ -24,13 +38,13 @@ def to_bits(t):
     return t.view(torch.int32).cpu().numpy().view(np.uint32)
 
 
-def gpu_compress(bits, flags=0):
+def gpu_compress(bits, flags=0, dtype=None):
     """Compress through the C ABI.  Returns (container bytes, device status)."""
     import torch
 
     import lossless_float_tensor_gb300 as uz
 
-    d = dtype_of(bits)
+    d = dtype_of(bits) if dtype is None else dtype
     n = bits.size
     x = to_device(bits) if n else None
     cap = uz.uzip_max_compressed_size(d, n)
@@ -53,7 +67,7 @@ def gpu_decompress(comp, dtype, n, capacity=None):
 
     c = torch.from_numpy(np.ascontiguousarray(comp)).cuda() if comp.size else torch.zeros(16, dtype=torch.uint8, device="cuda")
     cap = comp.size if capacity is None else capacity
-    es = 2 if dtype == BF16 else 4
+    es = ELEM_BYTES[dtype]
     out = torch.full((max(n, 1) * es,), 0xA5, dtype=torch.uint8, device="cuda")
     status = torch.full((), -1, dtype=torch.int32, device="cuda")
     st = uz.uzip_decompress(c.data_ptr(), cap, out.data_ptr(), dtype, n, status.data_ptr(),
@@ -62,4 +76,4 @@ def gpu_decompress(comp, dtype, n, capacity=None):
         return None, st
     torch.cuda.synchronize()
     raw = out.cpu().numpy()[: n * es]
-    return raw.view(np.uint16 if dtype == BF16 else np.uint32), int(status.item())
+    return raw.view(BITS[dtype]), int(status.item())

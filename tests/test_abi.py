@@ -42,7 +42,7 @@ def test_exports_every_declared_symbol(uz):
 
 
 def test_max_compressed_size_is_container_bound_plus_work_area(uz):
-    for dtype in (0, 1):
+    for dtype in range(5):  # bf16, fp32, fp16, fp8 e4m3fn, fp8 e5m2
         for n in [0, 1, 15, 16, 17, 65535, 65536, 65537, 3 * 65536 + 5, 1 << 29]:
             c = -(-n // 65536)
             bound = oracle.container_bound(dtype, n)
@@ -99,5 +99,5 @@ def test_host_argument_checks(uz):
     assert uz.uzip_compress_ex(fake, 0, 10, fake, 1 << 20, None, None, 8, 0) == uz.UZIP_ERR_INVALID_ARG
     assert uz.uzip_decompress(fake, 32, fake, 0, 10, None, 0) == uz.UZIP_ERR_CORRUPT
     assert uz.uzip_decompress(None, 1 << 20, fake, 0, 10, None, 0) == uz.UZIP_ERR_INVALID_ARG
-    assert uz.uzip_decompress(fake, 1 << 20, fake, 3, 10, None, 0) == uz.UZIP_ERR_UNSUPPORTED_DTYPE
+    assert uz.uzip_decompress(fake, 1 << 20, fake, 5, 10, None, 0) == uz.UZIP_ERR_UNSUPPORTED_DTYPE
     assert uz.uzip_query_size(None, 0)[0] == uz.UZIP_ERR_INVALID_ARG

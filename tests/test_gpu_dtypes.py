@@ -1,0 +1,89 @@
+"""GPU path against the oracle for fp16 and the two fp8 formats (the dtype
+sweep of UCCL-Zip Fig. 12): containers equal byte for byte, round trips
+bit-exact.  All calls go through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+NEW = [gu.FP16, gu.FP8_E4M3, gu.FP8_E5M2]
+NAMES = {gu.FP16: "fp16", gu.FP8_E4M3: "e4m3", gu.FP8_E5M2: "e5m2"}
+
+
+def _normal(code, n, std=0.02, tensor=0):
+    if code == gu.FP16:
+        return synth.normal_fp16(n, std, tensor=tensor)
+    return synth.normal_fp8(n, NAMES[code], std, tensor=tensor)
+
+
+def _random_bits(code, n, seed):
+    rng = np.random.default_rng(seed)
+    if code == gu.FP16:
+        return rng.integers(0, 1 << 16, n).astype(np.uint16).view(np.float16)
+    return rng.integers(0, 256, n).astype(np.uint8)
+
+
+def _parity(bits, code):
+    want = oracle.compress(bits, code)
+    got, status = gu.gpu_compress(bits, dtype=code)
+    assert status == 0
+    assert got.size == want.size, (got.size, want.size)
+    if not np.array_equal(got, want):
+        bad = np.flatnonzero(got != want)
+        raise AssertionError(f"{bad.size} bytes differ, first at {bad[0]} of {want.size}")
+    back, st = gu.gpu_decompress(want, code, bits.size)
+    assert st == 0
+    assert np.array_equal(back, bits.view(gu.BITS[code]))
+    return want
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 31, 33, 161, 1000, 4097, 65535, 65536, 65537, 131073])
+@pytest.mark.parametrize("code", NEW)
+def test_edge_sizes(code, n):
+    _parity(_normal(code, n, tensor=n % 7), code)
+
+
+@pytest.mark.parametrize("code", NEW)
+def test_all_patterns_and_chunk_kinds(code):
+    """Every bit pattern (NaN, infinities, subnormals, both zeros), then a
+    constant chunk, a random-bits chunk and a normal chunk with a ragged tail."""
+    if code == gu.FP16:
+        pats = np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16)
+        const = np.full(65536, 0x3C00, np.uint16).view(np.float16)
+    else:
+        pats = np.tile(np.arange(256, dtype=np.uint8), 256)
+        const = np.full(65536, 0x38, np.uint8)
+    bits = np.concatenate([pats, const, _random_bits(code, 65536, 5), _normal(code, 70001, tensor=3)])
+    comp = _parity(bits, code)
+    C = -(-bits.size // 65536)
+    lens = comp[64 + 8 * C:64 + 12 * C].view(np.uint32)
+    assert lens[1] == 162  # constant exponent: stream head plus one frequency
+
+
+@pytest.mark.parametrize("code", NEW)
+def test_large_normal(code):
+    comp = _parity(_normal(code, 1 << 24, tensor=9), code)
+    assert comp.size < (1 << 24) * gu.ELEM_BYTES[code]
+
+
+@pytest.mark.parametrize("code", NEW)
+def test_torch_round_trip(code):
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+
+    table = uz._torch_dtypes()
+    if code not in table:
+        pytest.skip("torch lacks this dtype")
+    bits = _normal(code, 300001, tensor=4)
+    x = torch.from_numpy(bits.view(gu.BITS[code]).view(np.uint8 if code != gu.FP16 else np.int16).copy()).cuda()
+    x = x.view(table[code])
+    buf, size = uz.compress(x)
+    comp = uz.compressed_bytes(buf, size)
+    assert np.array_equal(comp.cpu().numpy(), oracle.compress(bits, code))
+    y = uz.decompress(comp, table[code], x.numel())
+    assert torch.equal(y.view(torch.uint8), x.view(torch.uint8))

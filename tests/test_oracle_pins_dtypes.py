@@ -12,6 +12,13 @@ import pytest
 import oracle
 
 
+def _unpack(plane, n, w):
+    """The n w-bit fields of a plane packed least significant bit first
+    (numpy's own bit unpacking, independent of the oracle's loops)."""
+    bits = np.unpackbits(plane, bitorder="little")[: n * w].reshape(n, w).astype(np.int64)
+    return (bits << np.arange(w)).sum(axis=1)
+
+
 def _fields(e, rem, mbits):
     r = rem.astype(np.int64)
     return e.astype(np.int64), (r >> mbits) & 1, r & ((1 << mbits) - 1)
@@ -20,10 +27,9 @@ def _fields(e, rem, mbits):
 def test_fp16_all_patterns_roundtrip_and_ieee_value():
     x = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     e, r = oracle.split(x.view(np.float16))
-    assert r.size == 2 * x.size
+    assert r.size == 11 * x.size // 8
     assert np.array_equal(oracle.merge(oracle.FP16, e, r), x)
-    rem = r.view(np.uint16)
-    ex, sign, m = _fields(e, rem, 10)
+    ex, sign, m = _fields(e, _unpack(r, x.size, 11), 10)
     v = x.view(np.float16).astype(np.float64)
     assert np.array_equal(sign.astype(bool), np.signbit(v))
     fin = np.isfinite(v)
@@ -43,9 +49,9 @@ def test_fp8_all_patterns_match_torch_decoding(code, name, ebits, mbits, bias):
         pytest.skip(f"torch has no {name}")
     x = np.arange(256, dtype=np.uint8)
     e, r = oracle.split(x, code)
-    assert r.size == 128
+    assert r.size == 256 * (1 + mbits) // 8
     assert np.array_equal(oracle.merge(code, e, r), x)
-    nib = np.stack([r & 0xF, r >> 4], axis=1).reshape(-1)  # element 2j in the low nibble of byte j
+    nib = _unpack(r, 256, 1 + mbits)
     ex, sign, m = _fields(e, nib, mbits)
     assert np.all(ex < (1 << ebits)) and np.all(nib < (1 << (1 + mbits)))
     v = torch.from_numpy(x.copy()).view(getattr(torch, name)).float().double().numpy()
@@ -59,13 +65,28 @@ def test_fp8_all_patterns_match_torch_decoding(code, name, ebits, mbits, bias):
     assert np.array_equal(a, expect)
 
 
-def test_fp8_nibble_order_worked_example():
+def test_fp8_packing_worked_examples():
     """e4m3fn 1.0 (0x38), -1.5 (0xBC), NaN (0x7F): remainders 0, 1<<3|4, 7;
-    element 0 in the low nibble of byte 0, element 2 alone in byte 1."""
+    element 0 in the low nibble of byte 0, element 2 alone in byte 1.
+    e5m2 1.0 (0x3C), -inf (0xFC), smallest subnormal (0x01): 3-bit
+    remainders 000, 100, 001 at bits 0-2, 3-5, 6-8: bytes 0x60, 0x00."""
     x = np.array([0x38, 0xBC, 0x7F], np.uint8)
     e, r = oracle.split(x, oracle.FP8_E4M3)
     assert list(e) == [7, 7, 15]
     assert list(r) == [0xC0, 0x07]
+    y = np.array([0x3C, 0xFC, 0x01], np.uint8)
+    e, r = oracle.split(y, oracle.FP8_E5M2)
+    assert list(e) == [15, 31, 0]
+    assert list(r) == [0x60, 0x00]
+
+
+def test_fp16_packing_worked_example():
+    """fp16 -2.5 (0xC100) and 1.0 (0x3C00): 11-bit remainders 0x500 and 0;
+    fields at bits 0-10 and 11-21, so bytes 0x00, 0x05, 0x00."""
+    x = np.array([0xC100, 0x3C00], np.uint16).view(np.float16)
+    e, r = oracle.split(x)
+    assert list(e) == [16, 15]
+    assert list(r) == [0x00, 0x05, 0x00]
 
 
 @pytest.mark.parametrize("code,n", [(oracle.FP16, 65536 * 2 + 5), (oracle.FP8_E4M3, 65536 + 7),
@@ -80,12 +101,12 @@ def test_constant_exponent_container_size_closed_form(code, n):
     if code == oracle.FP16:
         bits = (np.uint16(14 << 10) | rng.integers(0, 1 << 10, n).astype(np.uint16)
                 | (rng.integers(0, 2, n).astype(np.uint16) << 15))
-        plane = 2 * n
+        plane = -(-11 * n // 8)
     else:
         mb = 3 if code == oracle.FP8_E4M3 else 2
         bits = ((np.uint8(6) << mb) | rng.integers(0, 1 << mb, n).astype(np.uint8)
                 | (rng.integers(0, 2, n).astype(np.uint8) << 7)).astype(np.uint8)
-        plane = (n + 1) // 2
+        plane = -(-(1 + mb) * n // 8)
     C = -(-n // 65536)
     r16 = lambda v: -(-v // 16) * 16
     sizes = [min(65536, n - 65536 * c) for c in range(C)]
