@@ -233,6 +233,7 @@ def run_ours(args, rank, world, local_rank):
     dominant = roof_c if mc >= md else roof_d
     cpu = None if args.no_cpu_baseline else cpu_baseline(bits)
     pipe = None if args.no_pipeline else run_pipeline(args, dev)
+    sweep = None if args.no_dtypes else run_dtype_sweep(args, dev, peak)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -244,7 +245,8 @@ def run_ours(args, rank, world, local_rank):
         "ratio": total / in_bytes, "compressed_bytes": total,
         "roofline": dominant, "roofline_compress": roof_c, "roofline_decompress": roof_d,
         "clocks": clk.summary(), "e2e": e2e, "gpu_launches": 2 * args.steps,
-        "wall_s_timed_region": wall, "cpu_baseline": cpu, "pipeline": pipe, "kernel_source_hash": kernel_hash(),
+        "wall_s_timed_region": wall, "cpu_baseline": cpu, "pipeline": pipe, "dtype_sweep": sweep,
+        "kernel_source_hash": kernel_hash(),
     }
     return line
 
@@ -363,6 +365,67 @@ def run_pipeline(args, dev):
             "raw_d2h_gbs": full["raw_d2h_gbs"]}
 
 
+def run_dtype_sweep(args, dev, peak):
+    """The five element formats of UCCL-Zip Fig. 12 on one 256 MiB tensor
+    each, ~ N(0, 0.02) rounded to the format: compress and decompress GB/s of
+    input (CUDA events, mean of 5 launches after 3 warm-ups), the ratio, the
+    fraction of the HBM roofline, and whether the container equals the
+    oracle's byte for byte and the round trip is bit-exact."""
+    import numpy as np
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+    import oracle
+    import synth
+
+    nbytes = 256 << 20
+    gens = [("bf16", uz.UZIP_BF16, 2, lambda n: synth.normal_bf16(n, 0.02, 13, 0)),
+            ("fp16", uz.UZIP_FP16, 2, lambda n: synth.normal_fp16(n, 0.02, 13, 1)),
+            ("fp32", uz.UZIP_FP32, 4, lambda n: synth.normal_fp32(n, 0.02, 13, 2)),
+            ("fp8_e4m3fn", uz.UZIP_FP8_E4M3, 1, lambda n: synth.normal_fp8(n, "e4m3", 0.02, 13, 3)),
+            ("fp8_e5m2", uz.UZIP_FP8_E5M2, 1, lambda n: synth.normal_fp8(n, "e5m2", 0.02, 13, 4))]
+    stream = torch.cuda.Stream(dev)
+    sp = stream.cuda_stream
+    rows = []
+    for name, code, es, gen in gens:
+        n = nbytes // es
+        bits = gen(n)
+        x = torch.from_numpy(np.ascontiguousarray(bits).view(np.uint8)).to(dev)
+        cap = uz.uzip_max_compressed_size(code, n)
+        comp = torch.empty(cap, dtype=torch.uint8, device=dev)
+        size = torch.zeros((), dtype=torch.int64, device=dev)
+        out = torch.empty_like(x)
+        status = torch.zeros((), dtype=torch.int32, device=dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(5)]
+        with torch.cuda.stream(stream):
+            for k in range(3 + 5):
+                e = ev[k - 3] if k >= 3 else None
+                if e:
+                    e[0].record(stream)
+                st = uz.uzip_compress(x.data_ptr(), code, n, comp.data_ptr(), cap, size.data_ptr(), sp)
+                if e:
+                    e[1].record(stream)
+                st2 = uz.uzip_decompress(comp.data_ptr(), cap, out.data_ptr(), code, n, status.data_ptr(), sp)
+                if e:
+                    e[2].record(stream)
+                if st or st2:
+                    raise RuntimeError(f"{name}: uzip status {st} {st2}")
+        torch.cuda.synchronize(dev)
+        total = int(size.item())
+        exact = int(status.item()) == 0 and torch.equal(out, x)
+        want = oracle.compress(bits, code)
+        same = want.size == total and np.array_equal(comp[:total].cpu().numpy(), want)
+        mc = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        md = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+        moved = nbytes + total
+        rows.append({"dtype": name, "elements": n, "input_bytes": nbytes, "ratio": total / nbytes,
+                     "compress_gbs": nbytes / (mc / 1e3) / 1e9, "decompress_gbs": nbytes / (md / 1e3) / 1e9,
+                     "compress_frac": moved / (mc / 1e3) / 1e9 / peak, "decompress_frac": moved / (md / 1e3) / 1e9 / peak,
+                     "round_trip_exact": bool(exact), "oracle_bytes_equal": bool(same)})
+        del x, comp, out
+    return {"workload": "one 256 MiB tensor per format ~ N(0, 0.02) (UCCL-Zip Fig. 12 format sweep)", "rows": rows}
+
+
 def cpu_baseline(bits):
     """The oracle (single-threaded C) on the whole tensor, compress + decompress."""
     import oracle
@@ -413,6 +476,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-pipeline", action="store_true")
+    ap.add_argument("--no-dtypes", action="store_true", help="skip the fp16/fp32/fp8 format sweep")
     ap.add_argument("--pipeline-messages", type=int, default=8,
                     help="1 GiB messages sent through the split-send pipeline")
     ap.add_argument("--elements", type=int, default=None,

@@ -63,18 +63,12 @@ __device__ __forceinline__ uint32_t rem_field(const uint8_t* __restrict__ rem, u
     return (v >> sh) & ((1u << W) - 1u);
 }
 
+// RAW chunk of a byte-field format (bf16, fp32): 16 values per lane at a time
 template <int DT>
-__device__ void merge_raw(const uint8_t* __restrict__ ex, const uint8_t* __restrict__ rem, uint8_t* __restrict__ out,
+__device__ void merge_raw_bytes(const uint8_t* __restrict__ ex, const uint8_t* __restrict__ rem, uint8_t* __restrict__ out,
                           uint32_t n_c, uint32_t lane) {
-    constexpr uint32_t es = Fmt<DT>::kEs;
-    if constexpr (DT != UZIP_BF16 && DT != UZIP_FP32) {  // element by element
-        for (uint32_t i = lane; i < n_c; i += 32) {
-            const uint32_t v = merge_bits<DT>(ex[i], rem_field<DT>(rem, i));
-            if (es == 2) reinterpret_cast<uint16_t*>(out)[i] = uint16_t(v);
-            else out[i] = uint8_t(v);
-        }
-        return;
-    }
+    constexpr uint32_t rb = DT == UZIP_BF16 ? 1 : 3;
+    constexpr uint32_t es = DT == UZIP_BF16 ? 2 : 4;
     const uint32_t nfull = n_c / 16;
     for (uint32_t b = lane; b < nfull; b += 32) {
         const uint4 eq = *reinterpret_cast<const uint4*>(ex + 16 * uint64_t(b));
@@ -116,9 +110,23 @@ __device__ void merge_raw(const uint8_t* __restrict__ ex, const uint8_t* __restr
         }
     }
     for (uint32_t i = nfull * 16 + lane; i < n_c; i += 32) {
-        const uint32_t v = merge_bits<DT>(ex[i], rem_field<DT>(rem, i));
+        uint32_t r = rem[rb * uint64_t(i)];
+        if (DT == UZIP_FP32) r |= uint32_t(rem[3 * uint64_t(i) + 1]) << 8 | uint32_t(rem[3 * uint64_t(i) + 2]) << 16;
+        const uint32_t v = merge_bits<DT>(ex[i], r);
         if (es == 2) reinterpret_cast<uint16_t*>(out)[i] = uint16_t(v);
         else reinterpret_cast<uint32_t*>(out)[i] = v;
+    }
+}
+
+// RAW chunk of a packed-field format (fp16, fp8): element by element
+template <int DT>
+__device__ void merge_raw_packed(const uint8_t* __restrict__ ex, const uint8_t* __restrict__ rem,
+                                 uint8_t* __restrict__ out, uint32_t n_c, uint32_t lane) {
+    constexpr uint32_t es = Fmt<DT>::kEs;
+    for (uint32_t i = lane; i < n_c; i += 32) {
+        const uint32_t v = merge_bits<DT>(ex[i], rem_field<DT>(rem, i));
+        if (es == 2) reinterpret_cast<uint16_t*>(out)[i] = uint16_t(v);
+        else out[i] = uint8_t(v);
     }
 }
 
@@ -249,15 +257,16 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
         const uint32_t widx = pos + lane;
         return __ldg(words + (widx < wlast ? widx : wlast));
     };
-    // Packed formats: a step's 32 fields are W consecutive words; this lane's
-    // field starts at bit W lane of them and may run into the next word.
+    // A step's 32 fields are RB consecutive words (RB = field bits); this
+    // lane's field starts at bit RB lane of them and may run into the next
+    // word.
     constexpr uint32_t RB = Fmt<DT>::kRbits;
     const uint32_t lword = (RB * lane) >> 5, lsh = (RB * lane) & 31;
     const bool lstraddle = lsh + RB > 32;
     auto load_rem_full = [&](uint32_t t) -> uint32_t {  // t < 2048 of a full chunk
-        if constexpr (!Fmt<DT>::kPacked) {
+        if constexpr (DT == UZIP_BF16) {
             return rem_field<DT>(rem, 32 * t + lane);
-        } else {
+        } else {  // two word loads at most and a funnel shift (fp32's 3-byte fields too)
             const uint32_t* p = reinterpret_cast<const uint32_t*>(rem) + RB * t + lword;
             const uint32_t lo = __ldg(p);
             const uint32_t hi = lstraddle ? __ldg(p + 1) : 0u;
@@ -437,7 +446,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 28 / kDecWarps) decompress_ker
             const uint8_t* rem = h + rem_off + c * Fmt<DT>::kRemChunk;
             uint8_t* out = a.out + c * kChunk * es;
             if (raw) {
-                if (len == n_c) merge_raw<DT>(src, rem, out, n_c, lane);
+                if (len == n_c) {
+                    if constexpr (Fmt<DT>::kPacked) merge_raw_packed<DT>(src, rem, out, n_c, lane);
+                    else merge_raw_bytes<DT>(src, rem, out, n_c, lane);
+                }
                 else good = false;
             } else {
                 // the ring reads the stream in whole 16-byte lines

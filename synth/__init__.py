@@ -341,3 +341,14 @@ def normal_fp8(n: int, fmt: str, std: float = 0.02, cfg: int = 11, tensor: int =
         return round_to_fp8(normal(key, idx, 2, 0) * std, fmt)
 
     return _parallel_fill(np.empty(n, np.uint8), n, fn)
+
+
+def normal_fp32(n: int, std: float = 0.02, cfg: int = 12, tensor: int = 0, start: int = 0) -> np.ndarray:
+    """n fp32 ~ N(0, std), as uint32 bit patterns."""
+    key = stream_key(cfg, tensor)
+
+    def fn(lo, hi):
+        idx = np.arange(start + lo, start + hi, dtype=np.uint64)
+        return (normal(key, idx, 2, 0) * std).astype(np.float32).view(np.uint32)
+
+    return _parallel_fill(np.empty(n, np.uint32), n, fn)
