@@ -427,17 +427,20 @@ def run_dtype_sweep(args, dev, peak):
 
 
 def cpu_baseline(bits):
-    """The oracle (single-threaded C) on the whole tensor, compress + decompress."""
+    """The oracle (single-threaded C) on a bounded sample of the tensor (the
+    first 2048 chunks), compress + decompress."""
     import oracle
 
+    sample = bits[: 2048 * 65536]
     t0 = time.perf_counter()
-    c = oracle.compress(bits)
+    c = oracle.compress(sample)
     t1 = time.perf_counter()
-    oracle.decompress(c, oracle.BF16, bits.size)
+    oracle.decompress(c, oracle.BF16, sample.size)
     t2 = time.perf_counter()
-    return {"value": 2 * bits.size / (t2 - t0) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"whole workload ({bits.size} values), compress {t1 - t0:.2f} s + decompress {t2 - t1:.2f} s",
-            "compress_gbs": 2 * bits.size / (t1 - t0) / 1e9, "decompress_gbs": 2 * bits.size / (t2 - t1) / 1e9}
+    return {"value": 2 * sample.size / (t2 - t0) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {sample.size} values of the workload ({sample.size // 65536} chunks), "
+                      f"compress {t1 - t0:.2f} s + decompress {t2 - t1:.2f} s",
+            "compress_gbs": 2 * sample.size / (t1 - t0) / 1e9, "decompress_gbs": 2 * sample.size / (t2 - t1) / 1e9}
 
 
 def run_reference(args):
