@@ -69,6 +69,12 @@ def lib():
         L.orc_container_bound.restype = ctypes.c_uint64
         L.orc_remainder_plane_bytes.argtypes = [ctypes.c_int, ctypes.c_uint64]
         L.orc_remainder_plane_bytes.restype = ctypes.c_uint64
+        L.orc_compress_mode.argtypes = [ctypes.c_int, vp, ctypes.c_uint64, vp, ctypes.c_uint64, u64p, ctypes.c_int]
+        L.orc_compress_mode.restype = ctypes.c_int
+        L.orc_gate_sample_elems.argtypes = [ctypes.c_int, ctypes.c_uint64]
+        L.orc_gate_sample_elems.restype = ctypes.c_uint64
+        L.orc_gate_says_raw.argtypes = [vp, ctypes.c_uint32]
+        L.orc_gate_says_raw.restype = ctypes.c_int
         L.orc_compress.argtypes = [ctypes.c_int, vp, ctypes.c_uint64, vp, ctypes.c_uint64, u64p]
         L.orc_decompress.argtypes = [vp, ctypes.c_uint64, ctypes.c_int, ctypes.c_uint64, vp]
         for name in ("orc_split", "orc_merge", "orc_normalise", "orc_rans_encode", "orc_rans_decode",
@@ -197,17 +203,33 @@ def container_bound(dtype: int, n: int) -> int:
     return int(lib().orc_container_bound(dtype, n))
 
 
-def compress(bits: np.ndarray, dtype: int | None = None) -> np.ndarray:
+MODE_CHUNK, MODE_RAW, MODE_GATE = 0, 1, 2
+
+
+def compress(bits: np.ndarray, dtype: int | None = None, mode: int = MODE_CHUNK) -> np.ndarray:
     """Container bytes for an array of element bit patterns (see dtype_code;
-    fp8 needs dtype=FP8_E4M3 or FP8_E5M2 with uint8 bits)."""
+    fp8 needs dtype=FP8_E4M3 or FP8_E5M2 with uint8 bits).  mode: per-chunk
+    choice, whole-message RAW, or RAW when the gate's sample says so."""
     d, bits = _bits(bits, dtype)
     n = bits.size
     cap = container_bound(d, n)
     out = np.empty(max(cap, 1), np.uint8)
     total = ctypes.c_uint64(0)
     src = bits if n else np.zeros(1, bits.dtype)
-    _check(lib().orc_compress(d, _ptr(src), n, _ptr(out), cap, ctypes.byref(total)), "compress")
+    _check(lib().orc_compress_mode(d, _ptr(src), n, _ptr(out), cap, ctypes.byref(total), mode), "compress")
     return out[: total.value].copy()
+
+
+def gate_says_raw(bits: np.ndarray, dtype: int | None = None) -> bool:
+    """The gate's decision for a message: its sample's exponent bytes would be
+    stored RAW if coded as one chunk."""
+    d, bits = _bits(bits, dtype)
+    ns = int(lib().orc_gate_sample_elems(d, bits.size))
+    exps, _ = split(bits[:ns], d)
+    r = lib().orc_gate_says_raw(_ptr(exps if ns else np.zeros(1, np.uint8)), ns)
+    if r < 0:
+        raise OracleError(ERR_INVALID_ARG, "gate")
+    return bool(r)
 
 
 def decompress_status(comp: np.ndarray, dtype: int, n: int):

@@ -432,8 +432,35 @@ uint64_t orc_container_bound(int dtype, uint64_t n) {
     return bound;
 }
 
+/* R23: the gate's sample is the first min(n, 65536 / element bytes)
+ * elements (at most 64 KiB of input); the message goes RAW when that sample,
+ * coded as one chunk, would be stored RAW under R9. */
+uint64_t orc_gate_sample_elems(int dtype, uint64_t n) {
+    int ebits, mbits, es;
+    if (!layout(dtype, &ebits, &mbits, &es)) return 0;
+    uint64_t s = 65536u / (uint64_t)es;
+    return n < s ? n : s;
+}
+
+int orc_gate_says_raw(const uint8_t* exps, uint32_t n_s) {
+    if (n_s == 0) return 0;
+    uint8_t* tmp = (uint8_t*)malloc((size_t)n_s + 672u + 2u * (size_t)n_s);
+    if (!tmp) return -1;
+    uint32_t len = 0;
+    int raw = 0;
+    int st = orc_encode_chunk(exps, n_s, 0, tmp, &len, &raw);
+    free(tmp);
+    return st == ORC_OK ? raw : -1;
+}
+
 int orc_compress(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t cap,
                  uint64_t* total) {
+    return orc_compress_mode(dtype, in, n, out, cap, total, ORC_MODE_CHUNK);
+}
+
+int orc_compress_mode(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t cap,
+                      uint64_t* total, int mode) {
+    if (mode != ORC_MODE_CHUNK && mode != ORC_MODE_RAW && mode != ORC_MODE_GATE) return ORC_ERR_INVALID_ARG;
     if (!dtype_ok(dtype)) return ORC_ERR_UNSUPPORTED_DTYPE;
     if (num_chunks(n) > 0xFFFFFFFFull) return ORC_ERR_INVALID_ARG;
     if ((n > 0 && in == NULL) || out == NULL) return ORC_ERR_INVALID_ARG;
@@ -449,12 +476,27 @@ int orc_compress(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t c
     if (!exps) return ORC_ERR_INVALID_ARG;
     orc_split(dtype, in, n, exps, out + rem_offset);
 
+    int all_raw = mode == ORC_MODE_RAW;
+    if (mode == ORC_MODE_GATE) {
+        all_raw = orc_gate_says_raw(exps, (uint32_t)orc_gate_sample_elems(dtype, n));
+        if (all_raw < 0) {
+            free(exps);
+            return ORC_ERR_INVALID_ARG;
+        }
+    }
     uint64_t off = 0;
     for (uint64_t c = 0; c < c_count; ++c) {
         uint32_t n_c = chunk_elems(n, c);
         uint32_t len = 0;
         int raw = 0;
-        int st = orc_encode_chunk(exps + c * ORC_CHUNK_ELEMS, n_c, 0, out + exp_offset + off, &len, &raw);
+        int st = ORC_OK;
+        if (all_raw) { /* the chunk's exponent bytes, as R9 stores a RAW chunk */
+            memcpy(out + exp_offset + off, exps + c * ORC_CHUNK_ELEMS, n_c);
+            len = n_c;
+            raw = 1;
+        } else {
+            st = orc_encode_chunk(exps + c * ORC_CHUNK_ELEMS, n_c, 0, out + exp_offset + off, &len, &raw);
+        }
         if (st != ORC_OK) {
             free(exps);
             return st;

@@ -103,6 +103,22 @@ uint64_t orc_container_bound(int dtype, uint64_t n);
  * orc_container_bound(dtype, n). */
 int orc_compress(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t cap,
                  uint64_t* total);
+/* Whole-message modes (R23; survey next row 4, NCCLZ Sec. IV-C and Alg. 1:
+ * a message whose coding would not pay travels RAW):
+ *   ORC_MODE_CHUNK  coded or RAW per chunk (R9), as orc_compress
+ *   ORC_MODE_RAW    every chunk stored RAW
+ *   ORC_MODE_GATE   every chunk RAW if the gate's sample would be stored RAW
+ *                   (orc_gate_says_raw), else as ORC_MODE_CHUNK */
+#define ORC_MODE_CHUNK 0
+#define ORC_MODE_RAW 1
+#define ORC_MODE_GATE 2
+int orc_compress_mode(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t cap,
+                      uint64_t* total, int mode);
+/* The gate's sample: the first min(n, 65536 / element bytes) elements. */
+uint64_t orc_gate_sample_elems(int dtype, uint64_t n);
+/* 1 if these n_s exponent bytes, coded as one chunk, would be stored RAW
+ * (R9), 0 if coded, -1 on error. */
+int orc_gate_says_raw(const uint8_t* exps, uint32_t n_s);
 /* Decompress and validate (R12). */
 int orc_decompress(const uint8_t* comp, uint64_t comp_bytes, int dtype, uint64_t n, void* out);
 

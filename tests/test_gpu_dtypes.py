@@ -87,3 +87,62 @@ def test_torch_round_trip(code):
     assert np.array_equal(comp.cpu().numpy(), oracle.compress(bits, code))
     y = uz.decompress(comp, table[code], x.numel())
     assert torch.equal(y.view(torch.uint8), x.view(torch.uint8))
+
+
+@pytest.mark.parametrize("code", NEW)
+def test_corruptions_rejected_like_oracle(code):
+    from tests.test_oracle_pins import _corruptions
+
+    x = _normal(code, 3 * 65536 + 777, tensor=6)
+    comp = oracle.compress(x, code)
+    for name, (b, size) in _corruptions(comp, x.size, code).items():
+        want, _ = oracle.decompress_status(b[:size], code, x.size)
+        _, st = gu.gpu_decompress(b[:size], code, x.size)
+        assert want == oracle.ERR_CORRUPT, name
+        assert st == want, name
+
+
+@pytest.mark.parametrize("code", NEW)
+def test_noalloc_matches_regular(code):
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+
+    x = _normal(code, 9 * 65536 + 4321, tensor=8)
+    want = oracle.compress(x, code)
+    d = gu.to_device(x)
+    C = -(-x.size // 65536)
+    cap = uz.uzip_max_compressed_size(code, x.size) - 16 - 8 * C
+    out = torch.full((cap,), 0x5A, dtype=torch.uint8, device="cuda")
+    size = torch.full((), -1, dtype=torch.int64, device="cuda")
+    rc = uz.uzip_compress_noalloc(d.data_ptr(), code, x.size, out.data_ptr(), cap, size.data_ptr(), None,
+                                  torch.cuda.current_stream().cuda_stream)
+    assert rc == uz.UZIP_OK
+    torch.cuda.synchronize()
+    assert int(size.item()) == want.size
+    assert np.array_equal(out[: want.size].cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("code", NEW)
+def test_pipeline_send_sized(code):
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+
+    msgs = [_normal(code, (1 << 20) + 321, tensor=10), _normal(code, 3 * 65536, tensor=11)]
+    d_msgs = [gu.to_device(m) for m in msgs]
+    cap = uz.uzip_max_compressed_size(code, max(m.size for m in msgs))
+    banks = [torch.empty(cap, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    hb = [torch.zeros(cap, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    sizes = torch.zeros(len(msgs), dtype=torch.int64).pin_memory()
+    s0, s1 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    st = uz.uzip_pipeline_send(code, [t.data_ptr() for t in d_msgs], [m.size for m in msgs], [b.data_ptr() for b in banks],
+                               cap, [h.data_ptr() for h in hb], cap, sizes.data_ptr(), uz.UZIP_PIPE_SIZED,
+                               s0.cuda_stream, s1.cuda_stream)
+    assert st == 0, uz.uzip_status_string(st)
+    torch.cuda.synchronize()
+    for k, m in enumerate(msgs):
+        want = oracle.compress(m, code)
+        assert int(sizes[k]) == want.size
+        assert np.array_equal(hb[k % 2].numpy()[: want.size], want)
