@@ -169,6 +169,23 @@ uzip_status uzip_compress_noalloc(const void* d_in, uzip_dtype dtype, uint64_t n
 uzip_status uzip_decompress(const void* d_comp, uint64_t comp_capacity, void* d_out,
                             uzip_dtype dtype, uint64_t n, int32_t* d_status, cudaStream_t s);
 
+/* Compression with a whole-message choice (NCCLZ Sec. IV-C and Alg. 1: a
+ * message whose coding would not pay travels RAW; it samples at most 64 KiB).
+ * The container format is the one above; only the choice differs:
+ *   - n * element bytes < raw_below_bytes: every chunk is stored RAW (no
+ *     statistics or coding; chunk c's RAW stream at offset 65536 c);
+ *   - otherwise the first min(n, 65536 / element bytes) elements (64 KiB of
+ *     input) are a sample: their exponent bytes are counted, normalised and
+ *     coded as one chunk on the device; if that chunk would be stored RAW
+ *     under the per-chunk rule, every chunk of the message is stored RAW,
+ *     else each chunk is coded or RAW as in uzip_compress.
+ * raw_below_bytes = 0 leaves the choice to the sample; UINT64_MAX forces RAW.
+ * Arguments, capacity (uzip_max_compressed_size), d_out_size and d_status
+ * are as for uzip_compress_ex; the decision never leaves the device. */
+uzip_status uzip_compress_gated(const void* d_in, uzip_dtype dtype, uint64_t n, void* d_out,
+                                uint64_t out_capacity, uint64_t* d_out_size, int32_t* d_status,
+                                uint64_t raw_below_bytes, cudaStream_t s);
+
 /* Read the 64-byte header of the container at d_comp (device) and return
  * its total size, dtype and element count.  Synchronises s.  Returns
  * UZIP_ERR_CORRUPT if the magic, version or layout fields do not check out,

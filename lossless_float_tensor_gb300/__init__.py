@@ -45,6 +45,8 @@ _lib.uzip_compress_ex.argtypes = [_vp, _int, _u64, _vp, _u64, _vp, _vp, _u32, _v
 _lib.uzip_compress_ex.restype = _int
 _lib.uzip_compress_noalloc.argtypes = [_vp, _int, _u64, _vp, _u64, _vp, _vp, _vp]
 _lib.uzip_compress_noalloc.restype = _int
+_lib.uzip_compress_gated.argtypes = [_vp, _int, _u64, _vp, _u64, _vp, _vp, _u64, _vp]
+_lib.uzip_compress_gated.restype = _int
 _lib.uzip_decompress.argtypes = [_vp, _u64, _vp, _int, _u64, _vp, _vp]
 _lib.uzip_decompress.restype = _int
 _lib.uzip_query_size.argtypes = [_vp, ctypes.POINTER(_u64), ctypes.POINTER(_int), ctypes.POINTER(_u64), _vp]
@@ -79,6 +81,12 @@ def uzip_compress(d_in: int, dtype: int, n: int, d_out: int, out_capacity: int, 
 def uzip_compress_ex(d_in: int, dtype: int, n: int, d_out: int, out_capacity: int, d_out_size: int | None,
                      d_status: int | None, flags: int, stream: int) -> int:
     return int(_lib.uzip_compress_ex(d_in, dtype, n, d_out, out_capacity, d_out_size, d_status, flags, stream))
+
+
+def uzip_compress_gated(d_in: int, dtype: int, n: int, d_out: int, out_capacity: int, d_out_size: int | None,
+                        d_status: int | None, raw_below_bytes: int, stream: int) -> int:
+    return int(_lib.uzip_compress_gated(d_in, dtype, n, d_out, out_capacity, d_out_size, d_status, raw_below_bytes,
+                                        stream))
 
 
 def uzip_compress_noalloc(d_in: int, dtype: int, n: int, d_out: int, out_capacity: int, d_out_size: int | None,

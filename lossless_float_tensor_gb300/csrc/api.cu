@@ -127,6 +127,27 @@ uzip_status uzip_compress(const void* d_in, uzip_dtype dtype, uint64_t n, void* 
     return uzip_compress_ex(d_in, dtype, n, d_out, out_capacity, d_out_size, nullptr, 0, s);
 }
 
+uzip_status uzip_compress_gated(const void* d_in, uzip_dtype dtype, uint64_t n, void* d_out, uint64_t out_capacity,
+                                uint64_t* d_out_size, int32_t* d_status, uint64_t raw_below_bytes, cudaStream_t s) {
+    if (!valid_dtype(dtype)) return UZIP_ERR_UNSUPPORTED_DTYPE;
+    if (n > UZIP_MAX_ELEMS) return UZIP_ERR_INVALID_ARG;
+    if (n > 0 && (d_in == nullptr || !aligned(d_in, 16))) return UZIP_ERR_INVALID_ARG;
+    if (d_out == nullptr || !aligned(d_out, 16)) return UZIP_ERR_INVALID_ARG;
+    if (d_out_size && !aligned(d_out_size, 8)) return UZIP_ERR_INVALID_ARG;
+    if (d_status && !aligned(d_status, 4)) return UZIP_ERR_INVALID_ARG;
+    const uint64_t need = uzip_max_compressed_size(dtype, n);
+    if (out_capacity < need) return UZIP_ERR_CAPACITY;
+    if (!device_range_ok(d_in, n * elem_bytes(dtype)) || !device_range_ok(d_out, need) ||
+        (d_out_size && !device_range_ok(d_out_size, 8)) || (d_status && !device_range_ok(d_status, 4)))
+        return UZIP_ERR_INVALID_ARG;
+    const int mode = n * elem_bytes(dtype) < raw_below_bytes ? 1 : 2;
+    if (launch_compress(dtype, d_in, n, d_out, d_out_size, d_status, 0, s, mode) != cudaSuccess) {
+        cudaGetLastError();
+        return UZIP_ERR_CUDA;
+    }
+    return UZIP_OK;
+}
+
 uzip_status uzip_compress_noalloc(const void* d_in, uzip_dtype dtype, uint64_t n, void* d_out, uint64_t out_capacity,
                                   uint64_t* d_out_size, int32_t* d_status, cudaStream_t s) {
     if (!valid_dtype(dtype)) return UZIP_ERR_UNSUPPORTED_DTYPE;

@@ -35,6 +35,7 @@ struct CompressArgs {
     uint8_t* stash;       // nullable: two slots of kSlotBytes per warp (exponent bytes, then the stream)
     uint32_t first_ticket;
     uint32_t num_chunks;
+    uint32_t gated;  // 1: a gate kernel ran first; scratch->pad = 1 means the whole message goes RAW
 };
 
 // element traits --------------------------------------------------------------
@@ -79,11 +80,12 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t lane, ui
 // l mod 16 (16 KiB in all).  Lanes l and l + 16 share a column, so the atomic
 // increments stay exact; within one instruction they meet only when both see
 // exponents of equal parity.
-template <int DT>
+// COUNT = false: the plane split alone (a whole-message RAW container).
+template <int DT, bool COUNT = true>
 __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* __restrict__ rem_dst,
                                 uint8_t* __restrict__ ex_dst, uint8_t* hist, uint32_t lane, uint64_t pol_keep,
                                 uint64_t pol_stream) {
-    {
+    if constexpr (COUNT) {
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll 8
         for (uint32_t i = lane; i < kRegionA / 16; i += 32) reinterpret_cast<uint4*>(hist)[i] = z;
@@ -91,7 +93,7 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
     __syncwarp();
     uint8_t* hl = hist + 4 * (lane & 15);
     auto count = [&](uint32_t e64) {  // e64 = exponent * 64
-        atomicAdd(reinterpret_cast<uint32_t*>(hl + e64), 1u);
+        if constexpr (COUNT) atomicAdd(reinterpret_cast<uint32_t*>(hl + e64), 1u);
     };
     // A unit is 16 consecutive values (32 bytes of bf16, 64 of fp32) handled by
     // one lane: its remainder bytes (16 or 48) and exponent bytes (16) leave as
@@ -197,20 +199,22 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
 // The same pass for formats whose sign|fraction field is not a whole number
 // of bytes (fp16: 11 bits, fp8 e4m3fn: 4, e5m2: 3): a unit is 32 values, whose
 // W-bit fields pack into exactly W 32-bit words, least significant bit first.
-template <int DT>
+template <int DT, bool COUNT = true>
 __device__ void split_and_count_packed(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* __restrict__ rem_dst,
                                        uint8_t* __restrict__ ex_dst, uint8_t* hist, uint32_t lane,
                                        uint64_t pol_stream) {
     static_assert(Fmt<DT>::kPacked, "packed-field formats only");
     constexpr uint32_t es = Fmt<DT>::kEs, mb = Fmt<DT>::kMbits, W = Fmt<DT>::kRbits;
-    {
+    if constexpr (COUNT) {
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll 8
         for (uint32_t i = lane; i < kRegionA / 16; i += 32) reinterpret_cast<uint4*>(hist)[i] = z;
     }
     __syncwarp();
     uint8_t* hl = hist + 4 * (lane & 15);
-    auto count = [&](uint32_t e64) { atomicAdd(reinterpret_cast<uint32_t*>(hl + e64), 1u); };
+    auto count = [&](uint32_t e64) {
+        if constexpr (COUNT) atomicAdd(reinterpret_cast<uint32_t*>(hl + e64), 1u);
+    };
     constexpr uint32_t PV = 2 * es;  // 16-byte vectors per 32-value unit
     const uint32_t nunits = n_c / 32;
     auto process = [&](const uint4 (&q)[PV], uint32_t unit) {
@@ -896,6 +900,31 @@ __device__ bool resolve_offset(uint64_t* desc, uint32_t c, uint64_t padded, uint
 }
 
 // ---------------------------------------------------------------------------
+// Header (R11) and the zero padding around the remainder plane; total = 0
+// marks a failed compression.  One thread.
+template <int DT>
+__device__ void write_header(const CompressArgs& a, uint64_t total, uint32_t st) {
+    const uint64_t n = a.n, C = a.num_chunks;
+    const uint64_t rem_off = C ? rem_offset(n) : kHeader, exp_off = C ? exp_offset(DT, n) : kHeader;
+    uint8_t* h = a.out;
+    *reinterpret_cast<uint32_t*>(h) = 0x31505A55u;  // "UZP1"
+    *reinterpret_cast<uint16_t*>(h + 4) = 1;
+    h[6] = uint8_t(DT);
+    h[7] = 0;
+    *reinterpret_cast<uint64_t*>(h + 8) = n;
+    *reinterpret_cast<uint32_t*>(h + 16) = kChunk;
+    *reinterpret_cast<uint32_t*>(h + 20) = uint32_t(C);
+    *reinterpret_cast<uint64_t*>(h + 24) = rem_off;
+    *reinterpret_cast<uint64_t*>(h + 32) = exp_off;
+    *reinterpret_cast<uint64_t*>(h + 40) = total;
+    *reinterpret_cast<uint64_t*>(h + 48) = 0;
+    *reinterpret_cast<uint64_t*>(h + 56) = 0;
+    for (uint64_t i = kHeader + 12 * C; i < rem_off; ++i) h[i] = 0;
+    for (uint64_t i = rem_off + rem_plane_bytes(DT, n); i < exp_off; ++i) h[i] = 0;
+    if (a.out_size) *a.out_size = total;
+    if (a.status_out) *a.status_out = int32_t(st ? st : (total ? 0u : uint32_t(UZIP_ERR_TIMEOUT)));
+}
+
 template <int DT>
 __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -914,6 +943,7 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
     // this warp's two slots (one warp per block)
     uint8_t* slots = a.stash ? a.stash + uint64_t(blockIdx.x) * 2 * kSlotBytes : nullptr;
     uint32_t which = 0;
+    if (a.gated && *reinterpret_cast<volatile uint32_t*>(&a.scratch->pad) != 0) return;  // the RAW kernel has it
 
     // Chunk c is placed: table entries, done counter; the warp that completes
     // the last chunk writes the header.  Returns true for that warp.
@@ -937,23 +967,7 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
             const uint64_t last = ld_acquire_u64(a.desc + (C - 1));
             uint64_t total = exp_off + (last & kDescValue);
             if (st != 0 || (last >> 62) != 2) total = 0;
-            uint8_t* h = a.out;
-            *reinterpret_cast<uint32_t*>(h) = 0x31505A55u;  // "UZP1"
-            *reinterpret_cast<uint16_t*>(h + 4) = 1;
-            h[6] = uint8_t(DT);
-            h[7] = 0;
-            *reinterpret_cast<uint64_t*>(h + 8) = n;
-            *reinterpret_cast<uint32_t*>(h + 16) = kChunk;
-            *reinterpret_cast<uint32_t*>(h + 20) = C;
-            *reinterpret_cast<uint64_t*>(h + 24) = rem_off;
-            *reinterpret_cast<uint64_t*>(h + 32) = exp_off;
-            *reinterpret_cast<uint64_t*>(h + 40) = total;
-            *reinterpret_cast<uint64_t*>(h + 48) = 0;
-            *reinterpret_cast<uint64_t*>(h + 56) = 0;
-            for (uint64_t i = kHeader + 12 * uint64_t(C); i < rem_off; ++i) h[i] = 0;
-            for (uint64_t i = rem_off + rem_plane_bytes(DT, n); i < exp_off; ++i) h[i] = 0;
-            if (a.out_size) *a.out_size = total;
-            if (a.status_out) *a.status_out = int32_t(st ? st : (total ? 0u : uint32_t(UZIP_ERR_TIMEOUT)));
+            write_header<DT>(a, total, st);
         }
         return true;
     };
@@ -1057,34 +1071,116 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
     }
     if (pend && place_pending()) return;
     // empty tensor: header only, written by the single launched warp
-    if (C == 0 && blockIdx.x == 0 && lane == 0) {
-        uint8_t* h = a.out;
-        *reinterpret_cast<uint32_t*>(h) = 0x31505A55u;
-        *reinterpret_cast<uint16_t*>(h + 4) = 1;
-        h[6] = uint8_t(DT);
-        h[7] = 0;
-        *reinterpret_cast<uint64_t*>(h + 8) = 0;
-        *reinterpret_cast<uint32_t*>(h + 16) = kChunk;
-        *reinterpret_cast<uint32_t*>(h + 20) = 0;
-        *reinterpret_cast<uint64_t*>(h + 24) = kHeader;
-        *reinterpret_cast<uint64_t*>(h + 32) = kHeader;
-        *reinterpret_cast<uint64_t*>(h + 40) = kHeader;
-        *reinterpret_cast<uint64_t*>(h + 48) = 0;
-        *reinterpret_cast<uint64_t*>(h + 56) = 0;
-        if (a.out_size) *a.out_size = kHeader;
-        if (a.status_out) *a.status_out = 0;
+    if (C == 0 && blockIdx.x == 0 && lane == 0) write_header<DT>(a, kHeader, 0);
+}
+
+// ---------------------------------------------------------------------------
+// Whole-message modes (NCCLZ Sec. IV-C, Alg. 1: a message whose coding would
+// not pay travels RAW).
+//
+// gate_kernel: one warp decides from the message's first 64 KiB of input --
+// the sample's exponent bytes counted, normalised and coded (count only) as
+// one chunk -- and sets scratch->pad = 1 when that chunk would be stored RAW
+// under the per-chunk rule.  It writes the sample's share of the remainder
+// plane as a side effect, with the bytes the main pass writes again.
+template <int DT>
+__global__ void __launch_bounds__(32) gate_kernel(CompressArgs a, uint32_t n_s) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint8_t* regA = smem;
+    uint8_t* regB = smem + kRegionA;
+    const uint32_t lane = threadIdx.x;
+    const uint64_t pol = policy_evict_first();
+    uint8_t* rem = a.out + rem_offset(a.n);
+    if constexpr (Fmt<DT>::kPacked)
+        split_and_count_packed<DT>(a.in, n_s, rem, nullptr, regA, lane, pol);
+    else
+        split_and_count<DT>(a.in, n_s, rem, nullptr, regA, lane, pol, pol);
+    uint32_t cnt[8];
+    reduce_hist(regA, lane, cnt);
+    __syncwarp();
+    Norm nm;
+    normalise(cnt, n_s, lane, regB, nm);
+    build_enc_table(nm, lane, regA, regB);
+    const uint32_t hdr = kStreamHead + 2 * nm.k_total;
+    EncState cs{kRansL, 0};
+    const bool coded = encode_chunk<DT, Sink::Count>(a.in, n_s, smem_addr(regA), lane, cs, nullptr, hdr, pol);
+    const bool raw = !coded || hdr + 2 * uint32_t(-cs.pos) >= n_s;
+    if (lane == 0) a.scratch->pad = raw ? 1u : 0u;
+}
+
+// raw_kernel: every chunk RAW.  Offsets need no look-back: chunk c's RAW
+// stream (its exponent bytes) starts at 65536 c of the exponent section.
+// Exits at once when a gate ran and chose coding.
+template <int DT>
+__global__ void __launch_bounds__(32) raw_kernel(CompressArgs a) {
+    if (a.gated && *reinterpret_cast<volatile uint32_t*>(&a.scratch->pad) == 0) return;
+    const uint32_t lane = threadIdx.x;
+    const uint64_t n = a.n, C = a.num_chunks;
+    const uint64_t rem_off = rem_offset(n), exp_off = exp_offset(DT, n);
+    const uint64_t pol = policy_evict_first();
+    for (uint64_t c = blockIdx.x; c < C; c += gridDim.x) {
+        const uint64_t left = n - c * kChunk;
+        const uint32_t n_c = uint32_t(left < kChunk ? left : kChunk);
+        const uint8_t* cin = a.in + c * kChunk * Fmt<DT>::kEs;
+        uint8_t* dst = a.out + exp_off + c * kChunk;
+        if constexpr (Fmt<DT>::kPacked)
+            split_and_count_packed<DT, false>(cin, n_c, a.out + rem_off + c * Fmt<DT>::kRemChunk, dst, nullptr, lane,
+                                              pol);
+        else
+            split_and_count<DT, false>(cin, n_c, a.out + rem_off + c * Fmt<DT>::kRemChunk, dst, nullptr, lane, pol,
+                                       pol);
+        for (uint32_t i = n_c + lane; i < round16(n_c); i += 32) dst[i] = 0;
+        if (lane == 0) {
+            reinterpret_cast<uint64_t*>(a.out + kHeader)[c] = c * kChunk;
+            reinterpret_cast<uint32_t*>(a.out + kHeader + 8 * C)[c] = n_c | kRawFlag;
+        }
     }
+    if (blockIdx.x == 0 && lane == 0) write_header<DT>(a, container_bound(DT, n), 0);
 }
 
 // ---------------------------------------------------------------------------
 // host launchers (called by the C ABI after argument checks)
+
+// Launches the kernels of one compression mode (0: per-chunk choice, 1: whole
+// message RAW, 2: gated) for element format DT.
+template <int DT>
+cudaError_t launch_mode(CompressArgs a, int mode, bool stash, cudaStream_t s) {
+    cudaError_t err;
+    const uint64_t n = a.n, C = a.num_chunks;
+    int sms = 0, per_sm = 0;
+    a.gated = mode == 2 ? 1u : 0u;
+    if (mode == 2 && n > 0) {
+        const uint64_t ns_max = 65536 / Fmt<DT>::kEs;  // 64 KiB of input
+        gate_kernel<DT><<<1, 32, kCompressSmem, s>>>(a, uint32_t(n < ns_max ? n : ns_max));
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    if (mode == 1 || (mode == 2 && n > 0)) {
+        if ((err = launch_shape(reinterpret_cast<const void*>(raw_kernel<DT>), 32, 0, &sms, &per_sm)) != cudaSuccess)
+            return err;
+        uint64_t grid = uint64_t(per_sm) * uint64_t(sms);
+        if (grid > C) grid = C;
+        if (grid < 1) grid = 1;
+        raw_kernel<DT><<<dim3(uint32_t(grid)), dim3(32), 0, s>>>(a);
+        if ((err = cudaGetLastError()) != cudaSuccess || mode == 1) return err;
+    }
+    void (*kern)(CompressArgs) = compress_kernel<DT>;
+    if ((err = launch_shape(reinterpret_cast<const void*>(kern), 32, kCompressSmem, &sms, &per_sm)) != cudaSuccess)
+        return err;
+    uint64_t grid = uint64_t(per_sm) * uint64_t(sms);
+    const uint64_t work = C > a.first_ticket ? C - a.first_ticket : 1;
+    if (grid > work) grid = work;
+    if (stash && grid > stash_warps(n)) grid = stash_warps(n);  // two slots per warp
+    if (grid < 1) grid = 1;
+    kern<<<dim3(uint32_t(grid)), dim3(32), kCompressSmem, s>>>(a);
+    return cudaGetLastError();
+}
 
 // Launches the compressor with its work area (status, ticket, done counter,
 // look-back descriptors: scratch_bytes(n) bytes) at `scratch`, which is
 // zeroed on `s` first.
 cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                                          int32_t* d_status, uint32_t first_ticket, void* scratch_area, void* stash,
-                                         cudaStream_t s) {
+                                         cudaStream_t s, int mode) {
     const uint64_t C = num_chunks(n);
     uint8_t* out = static_cast<uint8_t*>(d_out);
     Scratch* scratch = static_cast<Scratch*>(scratch_area);
@@ -1101,32 +1197,25 @@ cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n
     a.first_ticket = C > 0 ? (first_ticket < C ? first_ticket : uint32_t(C - 1)) : 0;
     a.num_chunks = uint32_t(C);
     a.stash = static_cast<uint8_t*>(stash);
-
-    void (*kern)(CompressArgs) = dtype == UZIP_BF16       ? compress_kernel<UZIP_BF16>
-                                 : dtype == UZIP_FP32     ? compress_kernel<UZIP_FP32>
-                                 : dtype == UZIP_FP16     ? compress_kernel<UZIP_FP16>
-                                 : dtype == UZIP_FP8_E4M3 ? compress_kernel<UZIP_FP8_E4M3>
-                                                          : compress_kernel<UZIP_FP8_E5M2>;
-    int sms = 0, per_sm = 0;
-    if ((err = launch_shape(reinterpret_cast<const void*>(kern), 32, kCompressSmem, &sms, &per_sm)) != cudaSuccess)
-        return err;
-    uint64_t grid = uint64_t(per_sm) * uint64_t(sms);
-    const uint64_t work = C > a.first_ticket ? C - a.first_ticket : 1;
-    if (grid > work) grid = work;
-    if (stash && grid > stash_warps(n)) grid = stash_warps(n);  // two slots per warp
-    if (grid < 1) grid = 1;
-    kern<<<dim3(uint32_t(grid)), dim3(32), kCompressSmem, s>>>(a);
-    return cudaGetLastError();
+    a.gated = 0;
+    const bool has_stash = stash != nullptr;
+    switch (dtype) {
+        case UZIP_BF16: return launch_mode<UZIP_BF16>(a, mode, has_stash, s);
+        case UZIP_FP32: return launch_mode<UZIP_FP32>(a, mode, has_stash, s);
+        case UZIP_FP16: return launch_mode<UZIP_FP16>(a, mode, has_stash, s);
+        case UZIP_FP8_E4M3: return launch_mode<UZIP_FP8_E4M3>(a, mode, has_stash, s);
+        default: return launch_mode<UZIP_FP8_E5M2>(a, mode, has_stash, s);
+    }
 }
 
 // The regular path: the work area (counters, descriptors, slots) sits in the
 // caller's output buffer, behind the largest possible container.
 cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
-                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s) {
+                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s, int mode) {
     uint8_t* work = static_cast<uint8_t*>(d_out) + scratch_offset(dtype, n);
     const uintptr_t st = (reinterpret_cast<uintptr_t>(work) + scratch_bytes(n) + 255) & ~uintptr_t(255);
     return launch_compress_with_scratch(dtype, d_in, n, d_out, d_out_size, d_status, first_ticket, work,
-                                        reinterpret_cast<void*>(st), s);
+                                        reinterpret_cast<void*>(st), s, mode);
 }
 
 // ---------------------------------------------------------------------------

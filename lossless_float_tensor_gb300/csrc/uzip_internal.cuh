@@ -231,11 +231,13 @@ __host__ __device__ inline DivMagic div_magic(uint32_t f) {
 cudaError_t launch_shape(const void* kern, int threads, size_t smem, int* sms, int* per_sm);
 
 // launchers (compress.cu, decompress.cu, pipeline.cu)
+// mode: 0 per-chunk choice, 1 whole message RAW, 2 gated (a one-warp kernel
+// decides from the first 64 KiB of input)
 cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
-                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s);
+                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s, int mode = 0);
 cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                                          int32_t* d_status, uint32_t first_ticket, void* scratch_area, void* stash,
-                                         cudaStream_t s);
+                                         cudaStream_t s, int mode = 0);
 
 // allocation-free compression: largest tensor and device count served by the
 // library's own work area
