@@ -234,6 +234,7 @@ def run_ours(args, rank, world, local_rank):
     cpu = None if args.no_cpu_baseline else cpu_baseline(bits)
     pipe = None if args.no_pipeline else run_pipeline(args, dev)
     sweep = None if args.no_dtypes else run_dtype_sweep(args, dev, peak)
+    gate = None if args.no_gate else run_gate(args, dev, x, n, peak)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -245,7 +246,7 @@ def run_ours(args, rank, world, local_rank):
         "ratio": total / in_bytes, "compressed_bytes": total,
         "roofline": dominant, "roofline_compress": roof_c, "roofline_decompress": roof_d,
         "clocks": clk.summary(), "e2e": e2e, "gpu_launches": 2 * args.steps,
-        "wall_s_timed_region": wall, "cpu_baseline": cpu, "pipeline": pipe, "dtype_sweep": sweep,
+        "wall_s_timed_region": wall, "cpu_baseline": cpu, "pipeline": pipe, "dtype_sweep": sweep, "gate": gate,
         "kernel_source_hash": kernel_hash(),
     }
     return line
@@ -365,6 +366,59 @@ def run_pipeline(args, dev):
             "raw_d2h_gbs": full["raw_d2h_gbs"]}
 
 
+def run_gate(args, dev, x, n, peak):
+    """Whole-message choice (uzip_compress_gated): on the c4 tensor the 64 KiB
+    sample codes, so the gated call costs the gate kernel on top of the usual
+    compression; on 1 GiB of random bf16 bits the sample goes RAW and the
+    whole message is split and stored RAW without statistics or coding.
+    CUDA events, mean of 5 launches after 3 warm-ups."""
+    import numpy as np
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+
+    cap = uz.uzip_max_compressed_size(uz.UZIP_BF16, n)
+    comp = torch.empty(cap, dtype=torch.uint8, device=dev)
+    size = torch.zeros((), dtype=torch.int64, device=dev)
+    stream = torch.cuda.Stream(dev)
+    sp = stream.cuda_stream
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+            for e0, e1 in ev:
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+
+    def run(t, raw_below=None):
+        if raw_below is None:
+            st = uz.uzip_compress(t.data_ptr(), uz.UZIP_BF16, n, comp.data_ptr(), cap, size.data_ptr(), sp)
+        else:
+            st = uz.uzip_compress_gated(t.data_ptr(), uz.UZIP_BF16, n, comp.data_ptr(), cap, size.data_ptr(), None,
+                                        raw_below, sp)
+        if st:
+            raise RuntimeError(f"uzip status {st}")
+
+    rows = {}
+    rows["c4_plain_ms"] = timed(lambda: run(x))
+    rows["c4_gated_ms"] = timed(lambda: run(x, 0))
+    rows["c4_gated_bytes"] = int(size.item())
+    rows["c4_forced_raw_ms"] = timed(lambda: run(x, 1 << 62))
+    rnd = torch.from_numpy(np.random.default_rng(17).integers(0, 1 << 16, n, dtype=np.uint16).view(np.int16)).to(dev)
+    rows["random_plain_ms"] = timed(lambda: run(rnd))
+    rows["random_gated_ms"] = timed(lambda: run(rnd, 0))
+    rows["random_gated_bytes"] = int(size.item())
+    rows["raw_frac_of_hbm"] = (4 * n) / (rows["random_gated_ms"] / 1e3) / 1e9 / peak
+    del rnd
+    return {"workload": "c4 (1 GiB bf16) and 1 GiB of random bf16 bits (numpy seed 17)", "unit": "ms per launch",
+            **rows}
+
+
 def run_dtype_sweep(args, dev, peak):
     """The five element formats of UCCL-Zip Fig. 12 on one 256 MiB tensor
     each, ~ N(0, 0.02) rounded to the format: compress and decompress GB/s of
@@ -480,6 +534,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-pipeline", action="store_true")
     ap.add_argument("--no-dtypes", action="store_true", help="skip the fp16/fp32/fp8 format sweep")
+    ap.add_argument("--no-gate", action="store_true", help="skip the whole-message RAW / gate measurement")
     ap.add_argument("--pipeline-messages", type=int, default=8,
                     help="1 GiB messages sent through the split-send pipeline")
     ap.add_argument("--elements", type=int, default=None,

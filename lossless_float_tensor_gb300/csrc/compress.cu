@@ -1079,10 +1079,11 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
 // not pay travels RAW).
 //
 // gate_kernel: one warp decides from the message's first 64 KiB of input --
-// the sample's exponent bytes counted, normalised and coded (count only) as
-// one chunk -- and sets scratch->pad = 1 when that chunk would be stored RAW
-// under the per-chunk rule.  It writes the sample's share of the remainder
-// plane as a side effect, with the bytes the main pass writes again.
+// the sample's exponent bytes counted, normalised and coded as one chunk --
+// and sets scratch->pad = 1 when that chunk would be stored RAW under the
+// per-chunk rule.  It writes the sample's share of the remainder plane as a
+// side effect, with the bytes the main pass writes again, and codes through
+// the first slot of the work area (free until the main pass starts).
 template <int DT>
 __global__ void __launch_bounds__(32) gate_kernel(CompressArgs a, uint32_t n_s) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -1091,10 +1092,11 @@ __global__ void __launch_bounds__(32) gate_kernel(CompressArgs a, uint32_t n_s) 
     const uint32_t lane = threadIdx.x;
     const uint64_t pol = policy_evict_first();
     uint8_t* rem = a.out + rem_offset(a.n);
+    uint8_t* slot = a.stash;  // nullable
     if constexpr (Fmt<DT>::kPacked)
-        split_and_count_packed<DT>(a.in, n_s, rem, nullptr, regA, lane, pol);
+        split_and_count_packed<DT>(a.in, n_s, rem, slot, regA, lane, pol);
     else
-        split_and_count<DT>(a.in, n_s, rem, nullptr, regA, lane, pol, pol);
+        split_and_count<DT>(a.in, n_s, rem, slot, regA, lane, pol, pol);
     uint32_t cnt[8];
     reduce_hist(regA, lane, cnt);
     __syncwarp();
@@ -1103,8 +1105,14 @@ __global__ void __launch_bounds__(32) gate_kernel(CompressArgs a, uint32_t n_s) 
     build_enc_table(nm, lane, regA, regB);
     const uint32_t hdr = kStreamHead + 2 * nm.k_total;
     EncState cs{kRansL, 0};
-    const bool coded = encode_chunk<DT, Sink::Count>(a.in, n_s, smem_addr(regA), lane, cs, nullptr, hdr, pol);
-    const bool raw = !coded || hdr + 2 * uint32_t(-cs.pos) >= n_s;
+    bool raw;
+    if (slot && encode_slot(slot, n_s, smem_addr(regA), lane, cs)) {
+        raw = hdr + 2 * (kSlotBytes / 2 - uint32_t(cs.pos)) >= n_s;
+    } else {
+        cs = EncState{kRansL, 0};
+        const bool coded = encode_chunk<DT, Sink::Count>(a.in, n_s, smem_addr(regA), lane, cs, nullptr, hdr, pol);
+        raw = !coded || hdr + 2 * uint32_t(-cs.pos) >= n_s;
+    }
     if (lane == 0) a.scratch->pad = raw ? 1u : 0u;
 }
 
