@@ -75,6 +75,8 @@ def lib():
         L.orc_gate_sample_elems.restype = ctypes.c_uint64
         L.orc_gate_says_raw.argtypes = [vp, ctypes.c_uint32]
         L.orc_gate_says_raw.restype = ctypes.c_int
+        L.orc_sampled_counts.argtypes = [vp, ctypes.c_uint32, ctypes.c_int, vp]
+        L.orc_sampled_counts.restype = ctypes.c_uint32
         L.orc_compress.argtypes = [ctypes.c_int, vp, ctypes.c_uint64, vp, ctypes.c_uint64, u64p]
         L.orc_decompress.argtypes = [vp, ctypes.c_uint64, ctypes.c_int, ctypes.c_uint64, vp]
         for name in ("orc_split", "orc_merge", "orc_normalise", "orc_rans_encode", "orc_rans_decode",
@@ -203,13 +205,14 @@ def container_bound(dtype: int, n: int) -> int:
     return int(lib().orc_container_bound(dtype, n))
 
 
-MODE_CHUNK, MODE_RAW, MODE_GATE = 0, 1, 2
+MODE_CHUNK, MODE_RAW, MODE_GATE, MODE_SAMPLED = 0, 1, 2, 3
 
 
 def compress(bits: np.ndarray, dtype: int | None = None, mode: int = MODE_CHUNK) -> np.ndarray:
     """Container bytes for an array of element bit patterns (see dtype_code;
     fp8 needs dtype=FP8_E4M3 or FP8_E5M2 with uint8 bits).  mode: per-chunk
-    choice, whole-message RAW, or RAW when the gate's sample says so."""
+    choice, whole-message RAW, RAW when the gate's sample says so, or tables
+    built from a sample of each chunk."""
     d, bits = _bits(bits, dtype)
     n = bits.size
     cap = container_bound(d, n)
@@ -244,3 +247,11 @@ def decompress(comp: np.ndarray, dtype: int, n: int) -> np.ndarray:
     st, out = decompress_status(comp, dtype, n)
     _check(st, "decompress")
     return out
+
+
+def sampled_counts(exps: np.ndarray, ebits: int):
+    """R24 counts of one chunk's exponent bytes and their total."""
+    exps = np.ascontiguousarray(np.asarray(exps, np.uint8))
+    counts = np.zeros(256, np.uint32)
+    total = lib().orc_sampled_counts(_ptr(exps), exps.size, ebits, _ptr(counts))
+    return counts, int(total)

@@ -318,7 +318,31 @@ int orc_encode_chunk(const uint8_t* exps, uint32_t n_c, int force_coded,
     orc_histogram(exps, n_c, counts);
     int st = orc_normalise(counts, n_c, freq);
     if (st != ORC_OK) return st;
+    return orc_encode_chunk_freq(exps, n_c, freq, force_coded, out, len, raw);
+}
 
+/* R24: counts for a table built from a sample of the chunk (UCCL-Zip Fig. 5:
+ * each block samples and builds its own table): the chunk's elements at
+ * positions 0, 16, 32, ...; a symbol seen s times in the sample counts 16 s,
+ * and every symbol of the format's exponent range [0, 2^ebits) not seen
+ * counts 1, so that it can still be coded.  Returns the counts' total. */
+uint32_t orc_sampled_counts(const uint8_t* exps, uint32_t n_c, int ebits, uint32_t counts[256]) {
+    uint32_t seen[256];
+    for (int s = 0; s < 256; ++s) seen[s] = 0;
+    for (uint32_t i = 0; i < n_c; i += 16) seen[exps[i]] += 1;
+    uint32_t total = 0;
+    for (int s = 0; s < 256; ++s) {
+        if (seen[s] > 0) counts[s] = 16u * seen[s];
+        else counts[s] = s < (1 << ebits) ? 1u : 0u;
+        total += counts[s];
+    }
+    return total;
+}
+
+int orc_encode_chunk_freq(const uint8_t* exps, uint32_t n_c, const uint16_t freq[256], int force_coded,
+                          uint8_t* out, uint32_t* len, int* raw) {
+    if (n_c == 0 || n_c > ORC_CHUNK_ELEMS) return ORC_ERR_INVALID_ARG;
+    int st;
     uint32_t states[32];
     uint32_t n_words = 0;
     uint16_t* words = (uint16_t*)malloc((size_t)n_c * sizeof(uint16_t));
@@ -460,7 +484,8 @@ int orc_compress(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t c
 
 int orc_compress_mode(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t cap,
                       uint64_t* total, int mode) {
-    if (mode != ORC_MODE_CHUNK && mode != ORC_MODE_RAW && mode != ORC_MODE_GATE) return ORC_ERR_INVALID_ARG;
+    if (mode != ORC_MODE_CHUNK && mode != ORC_MODE_RAW && mode != ORC_MODE_GATE && mode != ORC_MODE_SAMPLED)
+        return ORC_ERR_INVALID_ARG;
     if (!dtype_ok(dtype)) return ORC_ERR_UNSUPPORTED_DTYPE;
     if (num_chunks(n) > 0xFFFFFFFFull) return ORC_ERR_INVALID_ARG;
     if ((n > 0 && in == NULL) || out == NULL) return ORC_ERR_INVALID_ARG;
@@ -494,6 +519,15 @@ int orc_compress_mode(int dtype, const void* in, uint64_t n, uint8_t* out, uint6
             memcpy(out + exp_offset + off, exps + c * ORC_CHUNK_ELEMS, n_c);
             len = n_c;
             raw = 1;
+        } else if (mode == ORC_MODE_SAMPLED) {
+            int ebits, mbits, es;
+            layout(dtype, &ebits, &mbits, &es);
+            uint32_t counts[256];
+            uint16_t freq[256];
+            const uint8_t* ce = exps + c * ORC_CHUNK_ELEMS;
+            uint32_t total = orc_sampled_counts(ce, n_c, ebits, counts);
+            st = orc_normalise(counts, total, freq);
+            if (st == ORC_OK) st = orc_encode_chunk_freq(ce, n_c, freq, 0, out + exp_offset + off, &len, &raw);
         } else {
             st = orc_encode_chunk(exps + c * ORC_CHUNK_ELEMS, n_c, 0, out + exp_offset + off, &len, &raw);
         }

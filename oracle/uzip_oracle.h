@@ -112,8 +112,17 @@ int orc_compress(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t c
 #define ORC_MODE_CHUNK 0
 #define ORC_MODE_RAW 1
 #define ORC_MODE_GATE 2
+#define ORC_MODE_SAMPLED 3 /* R24: each chunk's table from a sample of it */
 int orc_compress_mode(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t cap,
                       uint64_t* total, int mode);
+/* R24 sampled-table counts of one chunk (positions 0, 16, 32, ...; a seen
+ * symbol counts 16 x its sample count, an unseen one of [0, 2^ebits) counts
+ * 1); returns their total. */
+uint32_t orc_sampled_counts(const uint8_t* exps, uint32_t n_c, int ebits, uint32_t counts[256]);
+/* One chunk stream coded with the given table (every symbol of exps must have
+ * freq > 0); RAW unless shorter, as orc_encode_chunk. */
+int orc_encode_chunk_freq(const uint8_t* exps, uint32_t n_c, const uint16_t freq[256], int force_coded,
+                          uint8_t* out, uint32_t* len, int* raw);
 /* The gate's sample: the first min(n, 65536 / element bytes) elements. */
 uint64_t orc_gate_sample_elems(int dtype, uint64_t n);
 /* 1 if these n_s exponent bytes, coded as one chunk, would be stored RAW
