@@ -109,11 +109,19 @@ uzip_status uzip_compress(const void* d_in, uzip_dtype dtype, uint64_t n, void* 
 /* As uzip_compress, plus:
  *   d_status  device i32 (nullable): 0 on success, else a uzip_status
  *             (UZIP_ERR_TIMEOUT when a chunk's offset wait ran out).
- *   flags     0 for normal use.  UZIP_TESTFLAG_SKIP_CHUNK0 makes the chunk
- *             counter start at 1, so chunk 0 never publishes its length and
- *             every wait on it runs out (about a second): it exists only to
- *             test the timeout path; the container is then invalid. */
+ *   flags     0 for normal use.  UZIP_FLAG_SAMPLED_TABLES builds each
+ *             chunk's table from a sample of the chunk instead of its full
+ *             histogram (UCCL-Zip Fig. 5: every block samples and builds its
+ *             own table): the elements at positions 0, 16, 32, ... of the
+ *             chunk; a symbol seen s times counts 16 s, every unseen symbol
+ *             of the format's exponent range counts 1 (so all stay codable);
+ *             the container format is unchanged, the containers are a little
+ *             larger.  UZIP_TESTFLAG_SKIP_CHUNK0 makes the chunk counter
+ *             start at 1, so chunk 0 never publishes its length and every
+ *             wait on it runs out (about a second): it exists only to test
+ *             the timeout path; the container is then invalid. */
 #define UZIP_TESTFLAG_SKIP_CHUNK0 1u
+#define UZIP_FLAG_SAMPLED_TABLES 2u
 uzip_status uzip_compress_ex(const void* d_in, uzip_dtype dtype, uint64_t n, void* d_out,
                              uint64_t out_capacity, uint64_t* d_out_size, int32_t* d_status,
                              uint32_t flags, cudaStream_t s);

@@ -26,6 +26,7 @@ UZIP_ERR_CUDA = 6
 UZIP_ERR_TOO_LARGE = 7
 UZIP_NOALLOC_MAX_ELEMS = 1 << 30
 UZIP_TESTFLAG_SKIP_CHUNK0 = 1
+UZIP_FLAG_SAMPLED_TABLES = 2
 UZIP_PIPE_EXACT, UZIP_PIPE_BOUND, UZIP_PIPE_SERIAL, UZIP_PIPE_SIZED = 0, 1, 2, 3
 UZIP_MAX_ELEMS = 1 << 40
 CHUNK_ELEMS = 65536

@@ -108,14 +108,15 @@ uzip_status uzip_compress_ex(const void* d_in, uzip_dtype dtype, uint64_t n, voi
     if (d_out == nullptr || !aligned(d_out, 16)) return UZIP_ERR_INVALID_ARG;
     if (d_out_size && !aligned(d_out_size, 8)) return UZIP_ERR_INVALID_ARG;
     if (d_status && !aligned(d_status, 4)) return UZIP_ERR_INVALID_ARG;
-    if ((flags & ~UZIP_TESTFLAG_SKIP_CHUNK0) != 0) return UZIP_ERR_INVALID_ARG;
+    if ((flags & ~(UZIP_TESTFLAG_SKIP_CHUNK0 | UZIP_FLAG_SAMPLED_TABLES)) != 0) return UZIP_ERR_INVALID_ARG;
     const uint64_t need = uzip_max_compressed_size(dtype, n);
     if (out_capacity < need) return UZIP_ERR_CAPACITY;
     if (!device_range_ok(d_in, n * elem_bytes(dtype)) || !device_range_ok(d_out, need) ||
         (d_out_size && !device_range_ok(d_out_size, 8)) || (d_status && !device_range_ok(d_status, 4)))
         return UZIP_ERR_INVALID_ARG;
     const uint32_t first = (flags & UZIP_TESTFLAG_SKIP_CHUNK0) ? 1u : 0u;
-    if (launch_compress(dtype, d_in, n, d_out, d_out_size, d_status, first, s) != cudaSuccess) {
+    const int mode = (flags & UZIP_FLAG_SAMPLED_TABLES) ? 3 : 0;
+    if (launch_compress(dtype, d_in, n, d_out, d_out_size, d_status, first, s, mode) != cudaSuccess) {
         cudaGetLastError();
         return UZIP_ERR_CUDA;
     }

@@ -925,7 +925,10 @@ __device__ void write_header(const CompressArgs& a, uint64_t total, uint32_t st)
     if (a.status_out) *a.status_out = int32_t(st ? st : (total ? 0u : uint32_t(UZIP_ERR_TIMEOUT)));
 }
 
-template <int DT>
+// SAMPLED: each chunk's table from a sample of it (positions 0, 16, 32, ...;
+// a seen symbol counts 16 x its sample count, an unseen one of the format's
+// exponent range counts 1; UCCL-Zip Fig. 5), without the full histogram.
+template <int DT, bool SAMPLED = false>
 __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* regA = smem;
@@ -1002,17 +1005,43 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
 
         // 1. plane split + exponent bytes + histogram
         if constexpr (Fmt<DT>::kPacked)
-            split_and_count_packed<DT>(cin, n_c, a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk, slot, regA, lane,
-                                       pol_stream);
+            split_and_count_packed<DT, !SAMPLED>(cin, n_c, a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk, slot,
+                                                 regA, lane, pol_stream);
         else
-            split_and_count<DT>(cin, n_c, a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk, slot, regA, lane,
-                                pol_keep, pol_stream);
+            split_and_count<DT, !SAMPLED>(cin, n_c, a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk, slot, regA,
+                                          lane, pol_keep, pol_stream);
+        uint32_t total = n_c;  // counts' total
+        if constexpr (SAMPLED) {
+            // histogram of the sample: every 16th exponent, from the slot or the input
+            const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll 8
+            for (uint32_t i = lane; i < kRegionA / 16; i += 32) reinterpret_cast<uint4*>(regA)[i] = z;
+            __syncwarp();
+            uint8_t* hl = regA + 4 * (lane & 15);
+            for (uint32_t i = 16 * lane; i < n_c; i += 16 * 32) {
+                const uint32_t e = slot ? uint32_t(slot[i]) : Traits<DT>::exp_of(Traits<DT>::load(cin, i));
+                atomicAdd(reinterpret_cast<uint32_t*>(hl + 64 * e), 1u);
+            }
+            __syncwarp();
+        }
         uint32_t cnt[8];
         reduce_hist(regA, lane, cnt);
         __syncwarp();
+        if constexpr (SAMPLED) {
+            uint32_t part = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t sym = 8 * lane + k;
+                cnt[k] = cnt[k] ? 16 * cnt[k] : (sym < (1u << Fmt<DT>::kEbits) ? 1u : 0u);
+                part += cnt[k];
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
+            total = part;
+        }
         // 2. normalise + encode table
         Norm nm;
-        normalise(cnt, n_c, lane, regB, nm);
+        normalise(cnt, total, lane, regB, nm);
         build_enc_table(nm, lane, regA, regB);
         const uint32_t hdr = kStreamHead + 2 * nm.k_total;
 
@@ -1171,7 +1200,7 @@ cudaError_t launch_mode(CompressArgs a, int mode, bool stash, cudaStream_t s) {
         raw_kernel<DT><<<dim3(uint32_t(grid)), dim3(32), 0, s>>>(a);
         if ((err = cudaGetLastError()) != cudaSuccess || mode == 1) return err;
     }
-    void (*kern)(CompressArgs) = compress_kernel<DT>;
+    void (*kern)(CompressArgs) = mode == 3 ? compress_kernel<DT, true> : compress_kernel<DT, false>;
     if ((err = launch_shape(reinterpret_cast<const void*>(kern), 32, kCompressSmem, &sms, &per_sm)) != cudaSuccess)
         return err;
     uint64_t grid = uint64_t(per_sm) * uint64_t(sms);
