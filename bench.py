@@ -370,7 +370,8 @@ def run_gate(args, dev, x, n, peak):
     """Whole-message choice (uzip_compress_gated): on the c4 tensor the 64 KiB
     sample codes, so the gated call costs the gate kernel on top of the usual
     compression; on 1 GiB of random bf16 bits the sample goes RAW and the
-    whole message is split and stored RAW without statistics or coding.
+    whole message is split and stored RAW without statistics or coding.  Also
+    c4 with tables from a sample of each chunk (UZIP_FLAG_SAMPLED_TABLES).
     CUDA events, mean of 5 launches after 3 warm-ups."""
     import numpy as np
     import torch
@@ -414,6 +415,15 @@ def run_gate(args, dev, x, n, peak):
     rows["random_gated_ms"] = timed(lambda: run(rnd, 0))
     rows["random_gated_bytes"] = int(size.item())
     rows["raw_frac_of_hbm"] = (4 * n) / (rows["random_gated_ms"] / 1e3) / 1e9 / peak
+
+    def run_sampled():
+        st = uz.uzip_compress_ex(x.data_ptr(), uz.UZIP_BF16, n, comp.data_ptr(), cap, size.data_ptr(), None,
+                                 uz.UZIP_FLAG_SAMPLED_TABLES, sp)
+        if st:
+            raise RuntimeError(f"uzip status {st}")
+
+    rows["c4_sampled_tables_ms"] = timed(run_sampled)
+    rows["c4_sampled_tables_bytes"] = int(size.item())
     del rnd
     return {"workload": "c4 (1 GiB bf16) and 1 GiB of random bf16 bits (numpy seed 17)", "unit": "ms per launch",
             **rows}

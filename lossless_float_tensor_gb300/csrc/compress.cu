@@ -80,20 +80,24 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t lane, ui
 // l mod 16 (16 KiB in all).  Lanes l and l + 16 share a column, so the atomic
 // increments stay exact; within one instruction they meet only when both see
 // exponents of equal parity.
-// COUNT = false: the plane split alone (a whole-message RAW container).
-template <int DT, bool COUNT = true>
+// CM: which exponents are counted: 1 all, 2 those at positions 0, 16, 32, ...
+// of the chunk (a sampled table), 0 none (a whole-message RAW container).
+template <int DT, int CM = 1>
 __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* __restrict__ rem_dst,
                                 uint8_t* __restrict__ ex_dst, uint8_t* hist, uint32_t lane, uint64_t pol_keep,
                                 uint64_t pol_stream) {
-    if constexpr (COUNT) {
+    if constexpr (CM != 0) {
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll 8
         for (uint32_t i = lane; i < kRegionA / 16; i += 32) reinterpret_cast<uint4*>(hist)[i] = z;
     }
     __syncwarp();
     uint8_t* hl = hist + 4 * (lane & 15);
-    auto count = [&](uint32_t e64) {  // e64 = exponent * 64
-        if constexpr (COUNT) atomicAdd(reinterpret_cast<uint32_t*>(hl + e64), 1u);
+    // e64 = exponent * 64; pos = the value's position in its 16-value unit
+    auto count = [&](uint32_t e64, uint32_t pos) {
+        if constexpr (CM == 1) atomicAdd(reinterpret_cast<uint32_t*>(hl + e64), 1u);
+        if constexpr (CM == 2)
+            if (pos == 0) atomicAdd(reinterpret_cast<uint32_t*>(hl + e64), 1u);
     };
     // A unit is 16 consecutive values (32 bytes of bf16, 64 of fp32) handled by
     // one lane: its remainder bytes (16 or 48) and exponent bytes (16) leave as
@@ -117,8 +121,8 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
                 for (int j = 0; j < 4; ++j) {
                     r[4 * v + j] = ((w[j] >> (15 - mb)) & sgn) | (w[j] & frac);
                     eb[j] = (w[j] >> mb) & em2;
-                    count((eb[j] << 6) & 0x3FC0u);
-                    count((eb[j] >> 10) & 0x3FC0u);
+                    count((eb[j] << 6) & 0x3FC0u, 8 * v + 2 * j);
+                    count((eb[j] >> 10) & 0x3FC0u, 8 * v + 2 * j + 1);
                 }
                 ex[2 * v] = __byte_perm(eb[0], eb[1], 0x6420);
                 ex[2 * v + 1] = __byte_perm(eb[2], eb[3], 0x6420);
@@ -135,7 +139,7 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     r[4 * v + j] = (w[j] & 0x7FFFFFu) | ((w[j] >> 8) & 0x800000u);
-                    count((w[j] >> 17) & 0x3FC0u);
+                    count((w[j] >> 17) & 0x3FC0u, 4 * v + j);
                 }
                 ex[v] = ((w[0] >> 23) & 0xFFu) | ((w[1] >> 15) & 0xFF00u) | ((w[2] >> 7) & 0xFF0000u) |
                         ((w[3] << 1) & 0xFF000000u);
@@ -190,7 +194,7 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
         const uint32_t e = Traits<DT>::exp_of(b);
 #pragma unroll
         for (uint32_t k = 0; k < es - 1; ++k) rem_dst[(es - 1) * uint64_t(i) + k] = uint8_t(r >> (8 * k));
-        count(e << 6);
+        count(e << 6, i & 15u);
         if (ex_dst) ex_dst[i] = uint8_t(e);
     }
     __syncwarp();
@@ -199,21 +203,23 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
 // The same pass for formats whose sign|fraction field is not a whole number
 // of bytes (fp16: 11 bits, fp8 e4m3fn: 4, e5m2: 3): a unit is 32 values, whose
 // W-bit fields pack into exactly W 32-bit words, least significant bit first.
-template <int DT, bool COUNT = true>
+template <int DT, int CM = 1>
 __device__ void split_and_count_packed(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* __restrict__ rem_dst,
                                        uint8_t* __restrict__ ex_dst, uint8_t* hist, uint32_t lane,
                                        uint64_t pol_stream) {
     static_assert(Fmt<DT>::kPacked, "packed-field formats only");
     constexpr uint32_t es = Fmt<DT>::kEs, mb = Fmt<DT>::kMbits, W = Fmt<DT>::kRbits;
-    if constexpr (COUNT) {
+    if constexpr (CM != 0) {
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll 8
         for (uint32_t i = lane; i < kRegionA / 16; i += 32) reinterpret_cast<uint4*>(hist)[i] = z;
     }
     __syncwarp();
     uint8_t* hl = hist + 4 * (lane & 15);
-    auto count = [&](uint32_t e64) {
-        if constexpr (COUNT) atomicAdd(reinterpret_cast<uint32_t*>(hl + e64), 1u);
+    auto count = [&](uint32_t e64, uint32_t pos) {  // pos: position in the 32-value unit, mod 16
+        if constexpr (CM == 1) atomicAdd(reinterpret_cast<uint32_t*>(hl + e64), 1u);
+        if constexpr (CM == 2)
+            if (pos == 0) atomicAdd(reinterpret_cast<uint32_t*>(hl + e64), 1u);
     };
     constexpr uint32_t PV = 2 * es;  // 16-byte vectors per 32-value unit
     const uint32_t nunits = n_c / 32;
@@ -228,8 +234,8 @@ __device__ void split_and_count_packed(const uint8_t* __restrict__ cin, uint32_t
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const uint32_t eb = (w[j] >> mb) & em2;  // both exponents, bytes 0 and 2
-                count((eb << 6) & 0x3FC0u);
-                count((eb >> 10) & 0x3FC0u);
+                count((eb << 6) & 0x3FC0u, (2 * j) & 15);
+                count((eb >> 10) & 0x3FC0u, (2 * j + 1) & 15);
                 f[2 * j] = Traits<DT>::rem_of(w[j] & 0xFFFFu);
                 f[2 * j + 1] = Traits<DT>::rem_of(w[j] >> 16);
                 if (j & 1) ex[j >> 1] = __byte_perm((w[j - 1] >> mb) & em2, eb, 0x6420);
@@ -239,10 +245,10 @@ __device__ void split_and_count_packed(const uint8_t* __restrict__ cin, uint32_t
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 ex[j] = (w[j] >> mb) & em4;
-                count((ex[j] << 6) & 0x3FC0u);
-                count((ex[j] >> 2) & 0x3FC0u);
-                count((ex[j] >> 10) & 0x3FC0u);
-                count((ex[j] >> 18) & 0x3FC0u);
+                count((ex[j] << 6) & 0x3FC0u, (4 * j) & 15);
+                count((ex[j] >> 2) & 0x3FC0u, (4 * j + 1) & 15);
+                count((ex[j] >> 10) & 0x3FC0u, (4 * j + 2) & 15);
+                count((ex[j] >> 18) & 0x3FC0u, (4 * j + 3) & 15);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) f[4 * j + k] = Traits<DT>::rem_of((w[j] >> (8 * k)) & 0xFFu);
             }
@@ -314,7 +320,7 @@ __device__ void split_and_count_packed(const uint8_t* __restrict__ cin, uint32_t
         }
         for (uint32_t i = i0 + lane; i < n_c; i += 32) {
             const uint32_t e = Traits<DT>::exp_of(Traits<DT>::load(cin, i));
-            count(e << 6);
+            count(e << 6, i & 15u);
             if (ex_dst) ex_dst[i] = uint8_t(e);
         }
     }
@@ -347,6 +353,9 @@ struct Norm {
     uint32_t k_total;  // present symbols overall
 };
 
+// CLOSED: the excess step of R5 in closed form (many boosted symbols, as in a
+// sampled table); otherwise one unit at a time.  Both give the same table.
+template <bool CLOSED = false>
 __device__ void normalise(const uint32_t c[8], uint32_t n_c, uint32_t lane, uint8_t* regB, Norm& nm) {
     uint16_t* freq = reinterpret_cast<uint16_t*>(regB);          // u16[256]
     uint32_t* keys = reinterpret_cast<uint32_t*>(regB + 512);    // u32[256]
@@ -400,20 +409,55 @@ __device__ void normalise(const uint32_t c[8], uint32_t n_c, uint32_t lane, uint
             if (cand & (1u << k)) nm.f[k] += freq[8 * lane + k];
         __syncwarp();
     } else if (total > kM) {
-        uint32_t excess = total - kM;
-        while (excess--) {
-            uint32_t best = 0;
+        if constexpr (CLOSED) {
+            // R5 takes the excess one at a time from the largest f (ties: the
+            // smaller symbol).  Its end state in closed form: with D(L) = sum over
+            // symbols of max(0, f - L), the smallest level L with D(L) <= excess
+            // caps every f at L, and the r = excess - D(L) smallest symbols at
+            // level L lose one more.
+            const uint32_t excess = total - kM;
+            auto drop = [&](uint32_t level) {
+                uint32_t d = 0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) d += nm.f[k] > level ? nm.f[k] - level : 0u;
+                return __reduce_add_sync(0xFFFFFFFFu, d);
+            };
+            uint32_t lo = 1, hi = kM;  // D(kM) = 0 <= excess < D(0) = total
+            while (lo < hi) {
+                const uint32_t mid = (lo + hi) / 2;
+                if (drop(mid) <= excess) hi = mid;
+                else lo = mid + 1;
+            }
+            const uint32_t level = lo, r = excess - drop(lo);
+            uint32_t at = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) at += nm.f[k] >= level ? 1u : 0u;
+            uint32_t dummy;
+            uint32_t idx = warp_excl_scan(at, lane, &dummy);  // symbols at the level, ascending
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const uint32_t key = (nm.f[k] << 8) | (255u - (8 * lane + k));
-                best = key > best ? key : best;
+                if (nm.f[k] >= level) {
+                    nm.f[k] = level - (idx < r ? 1u : 0u);
+                    ++idx;
+                }
             }
-            const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
-            const uint32_t s = 255u - (top & 0xFFu);
-            if ((s >> 3) == lane) {
+        } else {
+            // the same, one step at a time
+            uint32_t excess = total - kM;
+            while (excess--) {
+                uint32_t best = 0;
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    if (uint32_t(k) == (s & 7u)) nm.f[k] -= 1;
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t key = (nm.f[k] << 8) | (255u - (8 * lane + k));
+                    best = key > best ? key : best;
+                }
+                const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
+                const uint32_t s = 255u - (top & 0xFFu);
+                if ((s >> 3) == lane) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if (uint32_t(k) == (s & 7u)) nm.f[k] -= 1;
+                }
             }
         }
     }
@@ -426,6 +470,9 @@ __device__ void normalise(const uint32_t c[8], uint32_t n_c, uint32_t lane, uint
     regB[1536 + lane] = uint8_t(present);  // bitmap byte `lane` = symbols 8*lane..8*lane+7
     __syncwarp();
 }
+
+// division magic of every frequency, built at compile time
+__device__ const MagicTable g_magic = make_magic_table();
 
 // encode table row for each present symbol: {m, add} and {(f << 20) - 1, (M - f) | cum << 12 | sh << 27}
 __device__ void build_enc_table(const Norm& nm, uint32_t lane, uint8_t* table, uint8_t* regB) {
@@ -451,7 +498,8 @@ __device__ void build_enc_table(const Norm& nm, uint32_t lane, uint8_t* table, u
     for (uint32_t i = lane; i < nm.k_total; i += 32) {
         const uint32_t s = plist[i];
         const uint32_t f = freq[s];
-        const DivMagic dm = div_magic(f);
+        const MagicEntry me = g_magic.e[f];
+        const DivMagic dm{me.m, (me.add_sh >> 8) ? me.m : 0u, me.add_sh & 0xFFu, 1u};
         uint4 e;
         e.x = dm.m;
         e.y = dm.add;
@@ -1005,25 +1053,12 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
 
         // 1. plane split + exponent bytes + histogram
         if constexpr (Fmt<DT>::kPacked)
-            split_and_count_packed<DT, !SAMPLED>(cin, n_c, a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk, slot,
+            split_and_count_packed<DT, SAMPLED ? 2 : 1>(cin, n_c, a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk, slot,
                                                  regA, lane, pol_stream);
         else
-            split_and_count<DT, !SAMPLED>(cin, n_c, a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk, slot, regA,
+            split_and_count<DT, SAMPLED ? 2 : 1>(cin, n_c, a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk, slot, regA,
                                           lane, pol_keep, pol_stream);
         uint32_t total = n_c;  // counts' total
-        if constexpr (SAMPLED) {
-            // histogram of the sample: every 16th exponent, from the slot or the input
-            const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll 8
-            for (uint32_t i = lane; i < kRegionA / 16; i += 32) reinterpret_cast<uint4*>(regA)[i] = z;
-            __syncwarp();
-            uint8_t* hl = regA + 4 * (lane & 15);
-            for (uint32_t i = 16 * lane; i < n_c; i += 16 * 32) {
-                const uint32_t e = slot ? uint32_t(slot[i]) : Traits<DT>::exp_of(Traits<DT>::load(cin, i));
-                atomicAdd(reinterpret_cast<uint32_t*>(hl + 64 * e), 1u);
-            }
-            __syncwarp();
-        }
         uint32_t cnt[8];
         reduce_hist(regA, lane, cnt);
         __syncwarp();
@@ -1041,7 +1076,7 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
         }
         // 2. normalise + encode table
         Norm nm;
-        normalise(cnt, total, lane, regB, nm);
+        normalise<SAMPLED>(cnt, total, lane, regB, nm);
         build_enc_table(nm, lane, regA, regB);
         const uint32_t hdr = kStreamHead + 2 * nm.k_total;
 
@@ -1161,10 +1196,10 @@ __global__ void __launch_bounds__(32) raw_kernel(CompressArgs a) {
         const uint8_t* cin = a.in + c * kChunk * Fmt<DT>::kEs;
         uint8_t* dst = a.out + exp_off + c * kChunk;
         if constexpr (Fmt<DT>::kPacked)
-            split_and_count_packed<DT, false>(cin, n_c, a.out + rem_off + c * Fmt<DT>::kRemChunk, dst, nullptr, lane,
+            split_and_count_packed<DT, 0>(cin, n_c, a.out + rem_off + c * Fmt<DT>::kRemChunk, dst, nullptr, lane,
                                               pol);
         else
-            split_and_count<DT, false>(cin, n_c, a.out + rem_off + c * Fmt<DT>::kRemChunk, dst, nullptr, lane, pol,
+            split_and_count<DT, 0>(cin, n_c, a.out + rem_off + c * Fmt<DT>::kRemChunk, dst, nullptr, lane, pol,
                                        pol);
         for (uint32_t i = n_c + lane; i < round16(n_c); i += 32) dst[i] = 0;
         if (lane == 0) {

@@ -197,7 +197,7 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 struct DivMagic {
     uint32_t m, add, sh, ok;
 };
-__host__ __device__ inline DivMagic div_magic(uint32_t f) {
+__host__ __device__ constexpr inline DivMagic div_magic(uint32_t f) {
     DivMagic r{0u, 0u, 0u, 0u};
     if (f == 0 || f > kM) return r;
     uint32_t lg = 0;
@@ -224,6 +224,23 @@ __host__ __device__ inline DivMagic div_magic(uint32_t f) {
         r.ok = 1;
     }
     return r;
+}
+
+// div_magic of every f in [1, 4096], evaluated at compile time: {m, sh |
+// (add != 0) << 8} (add is 0 or m)
+struct MagicEntry {
+    uint32_t m, add_sh;
+};
+struct MagicTable {
+    MagicEntry e[kM + 1];
+};
+constexpr MagicTable make_magic_table() {
+    MagicTable t{};
+    for (uint32_t f = 1; f <= kM; ++f) {
+        const DivMagic d = div_magic(f);
+        t.e[f] = MagicEntry{d.m, d.sh | (d.add ? 256u : 0u)};
+    }
+    return t;
 }
 
 // SM count and resident blocks per SM of `kern` on the current device, looked
