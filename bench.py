@@ -30,8 +30,8 @@ sys.path.insert(0, ROOT)
 METRIC = "compress & decompress GB/s (input bytes), ratio, % of HBM roofline, 1 GB300"
 WORKLOAD = ("c4: bf16 activations [8, 8192, 8192] ~ 0.5*Student-t(4), 82 outlier channels x50, "
             "chunk 4096 random bits; 536,870,912 values (1 GiB)")
-KERNEL_SOURCES = ["lossless_float_tensor_gb300/csrc/compress.cu", "lossless_float_tensor_gb300/csrc/decompress.cu",
-                  "lossless_float_tensor_gb300/csrc/uzip_internal.cuh"]
+KERNEL_SOURCES = ["lossless_float_tensor_gb300/csrc/compress_kernels.cuh", "lossless_float_tensor_gb300/csrc/compress.cu",
+                  "lossless_float_tensor_gb300/csrc/decompress.cu", "lossless_float_tensor_gb300/csrc/uzip_internal.cuh"]
 
 
 def kernel_hash() -> str:
