@@ -305,9 +305,12 @@ def run_pipeline(args, dev):
     (bf16 ~ N(0, 0.02)) is sent `reps` times, and prefixes of it give the
     64 KiB .. 1 GiB size sweep.  Reported: input GB/s of the pipelined modes
     (exact-size copy kernel into mapped pinned memory; exact-size
-    cudaMemcpyAsync issued once the host has read the size; bound-size
-    cudaMemcpyAsync), of compress-then-copy on one stream (no overlap), and of a
-    plain device-to-host copy of the uncompressed bytes."""
+    cudaMemcpyAsync issued once the host has read the size; streamed copies of
+    finished remainder and stream runs while the message compresses;
+    bound-size cudaMemcpyAsync), of compress-then-copy on one stream (no
+    overlap), and of a plain device-to-host copy of the uncompressed bytes.
+    Also the latency of one 1 GiB message: from the call to the last byte on
+    the host, sized versus streamed."""
     import numpy as np
     import torch
 
@@ -319,11 +322,12 @@ def run_pipeline(args, dev):
     x = torch.from_numpy(msg.view(np.int16)).to(dev)
     cap = uz.uzip_max_compressed_size(uz.UZIP_BF16, n_max)
     banks = [torch.empty(cap, dtype=torch.uint8, device=dev) for _ in range(2)]
-    hb = [torch.empty(cap, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    hcap = cap + 16 * (-(-n_max // 65536))  # the streamed mode keeps progress words past the container
+    hb = [torch.empty(hcap, dtype=torch.uint8).pin_memory() for _ in range(2)]
     h_raw = torch.empty(2 * n_max, dtype=torch.uint8).pin_memory()
     s0, s1 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    modes = {"exact": uz.UZIP_PIPE_EXACT, "sized": uz.UZIP_PIPE_SIZED, "bound": uz.UZIP_PIPE_BOUND,
-             "serial": uz.UZIP_PIPE_SERIAL}
+    modes = {"exact": uz.UZIP_PIPE_EXACT, "sized": uz.UZIP_PIPE_SIZED, "streamed": uz.UZIP_PIPE_STREAMED,
+             "bound": uz.UZIP_PIPE_BOUND, "serial": uz.UZIP_PIPE_SERIAL}
     sizes = [1 << 15, 1 << 17, 1 << 19, 1 << 21, 1 << 23, 1 << 25, 1 << 27, n_max]  # values (64 KiB .. 1 GiB)
     sweep = []
     for n in sizes:
@@ -337,7 +341,7 @@ def run_pipeline(args, dev):
                 torch.cuda.synchronize(dev)
                 t0 = time.perf_counter()
                 st = uz.uzip_pipeline_send(uz.UZIP_BF16, [x.data_ptr()] * reps, [n] * reps,
-                                           [b.data_ptr() for b in banks], cap, [h.data_ptr() for h in hb], cap,
+                                           [b.data_ptr() for b in banks], cap, [h.data_ptr() for h in hb], hcap,
                                            hs.data_ptr(), mode, s0.cuda_stream, s1.cuda_stream)
                 torch.cuda.synchronize(dev)
                 dt = time.perf_counter() - t0
@@ -357,11 +361,29 @@ def run_pipeline(args, dev):
             dt = time.perf_counter() - t0
         row["raw_d2h_gbs"] = reps * 2 * n / dt / 1e9
         sweep.append(row)
+    # one 1 GiB message, from the call to its last byte on the host
+    hs1 = torch.zeros(1, dtype=torch.int64).pin_memory()
+    latency = {}
+    for name in ("sized", "streamed"):
+        best = float("inf")
+        for _ in range(3):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            st = uz.uzip_pipeline_send(uz.UZIP_BF16, [x.data_ptr()], [n_max], [b.data_ptr() for b in banks], cap,
+                                       [h.data_ptr() for h in hb], hcap, hs1.data_ptr(), modes[name], s0.cuda_stream,
+                                       s1.cuda_stream)
+            torch.cuda.synchronize(dev)
+            best = min(best, time.perf_counter() - t0)
+            if st != 0:
+                raise RuntimeError(f"pipeline status {st}")
+        latency[name + "_ms"] = best * 1e3
     full = sweep[-1]
-    return {"workload": "c5: first 1 GiB message of the Llama-3-8B-shaped bf16 parameter set ~ N(0, 0.02), "
+    return {"one_message_latency": latency,
+            "workload": "c5: first 1 GiB message of the Llama-3-8B-shaped bf16 parameter set ~ N(0, 0.02), "
                         f"sent {full['messages']} times; size sweep on its prefixes",
             "unit": "GB/s (input bytes, host wall clock incl. sync)", "sweep": sweep,
-            "exact_gbs": full["exact_gbs"], "sized_gbs": full["sized_gbs"], "bound_gbs": full["bound_gbs"],
+            "exact_gbs": full["exact_gbs"], "sized_gbs": full["sized_gbs"], "streamed_gbs": full["streamed_gbs"],
+            "bound_gbs": full["bound_gbs"],
             "serial_gbs": full["serial_gbs"],
             "raw_d2h_gbs": full["raw_d2h_gbs"]}
 

@@ -232,13 +232,28 @@ const char* uzip_status_string(uzip_status st);
  *                            bytes (the copy engine instead of SM stores; the
  *                            call then blocks until the last compression has
  *                            finished, while the copies still overlap it).
+ *                            UZIP_PIPE_STREAMED: each message's container
+ *                            travels while it is being compressed (UCCL-Zip
+ *                            Fig. 4 d, split-send at plane and chunk grain):
+ *                            the kernel posts, in mapped memory, when each
+ *                            chunk's remainder bytes are written and where
+ *                            each chunk's stream ends once placed; the host
+ *                            copies finished runs of 64 chunks of either
+ *                            with cudaMemcpyAsync as they appear, and the
+ *                            header and chunk table when the kernel is done.
+ *                            The host banks must then hold round16(container
+ *                            bound of the largest message) + 16 bytes per
+ *                            chunk of it (the progress words sit after the
+ *                            container); the call returns once every copy of
+ *                            the last message is enqueued.
  * Returns once all work is enqueued; the work ends when both streams drain.
  * The caller must not reuse the banks until then. */
 typedef enum {
     UZIP_PIPE_EXACT = 0,
     UZIP_PIPE_BOUND = 1,
     UZIP_PIPE_SERIAL = 2,
-    UZIP_PIPE_SIZED = 3
+    UZIP_PIPE_SIZED = 3,
+    UZIP_PIPE_STREAMED = 4
 } uzip_pipe_mode;
 
 uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d_msgs, const uint64_t* msg_elems,

@@ -21,7 +21,7 @@ extern template cudaError_t launch_mode<UZIP_FP8_E5M2>(CompressArgs, int, bool, 
 // zeroed on `s` first.
 cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                                          int32_t* d_status, uint32_t first_ticket, void* scratch_area, void* stash,
-                                         cudaStream_t s, int mode) {
+                                         cudaStream_t s, int mode, uint64_t* progress) {
     const uint64_t C = num_chunks(n);
     uint8_t* out = static_cast<uint8_t*>(d_out);
     Scratch* scratch = static_cast<Scratch*>(scratch_area);
@@ -39,6 +39,7 @@ cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n
     a.num_chunks = uint32_t(C);
     a.stash = static_cast<uint8_t*>(stash);
     a.gated = 0;
+    a.progress = progress;
     const bool has_stash = stash != nullptr;
     switch (dtype) {
         case UZIP_BF16: return launch_mode<UZIP_BF16>(a, mode, has_stash, s);
@@ -52,11 +53,11 @@ cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n
 // The regular path: the work area (counters, descriptors, slots) sits in the
 // caller's output buffer, behind the largest possible container.
 cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
-                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s, int mode) {
+                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s, int mode, uint64_t* progress) {
     uint8_t* work = static_cast<uint8_t*>(d_out) + scratch_offset(dtype, n);
     const uintptr_t st = (reinterpret_cast<uintptr_t>(work) + scratch_bytes(n) + 255) & ~uintptr_t(255);
     return launch_compress_with_scratch(dtype, d_in, n, d_out, d_out_size, d_status, first_ticket, work,
-                                        reinterpret_cast<void*>(st), s, mode);
+                                        reinterpret_cast<void*>(st), s, mode, progress);
 }
 
 // ---------------------------------------------------------------------------

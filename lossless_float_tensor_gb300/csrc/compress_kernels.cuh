@@ -39,6 +39,10 @@ struct CompressArgs {
     uint32_t first_ticket;
     uint32_t num_chunks;
     uint32_t gated;  // 1: a gate kernel ran first; scratch->pad = 1 means the whole message goes RAW
+    // nullable, mapped host memory: per chunk c, progress[2c] = 1 once its
+    // remainder plane is written and progress[2c + 1] = 2^63 | (end of its
+    // stream in the exponent section) once the stream is in place
+    uint64_t* progress;
 };
 
 // element traits --------------------------------------------------------------
@@ -953,6 +957,14 @@ inline __device__ bool resolve_offset(uint64_t* desc, uint32_t c, uint64_t padde
 // ---------------------------------------------------------------------------
 // Header (R11) and the zero padding around the remainder plane; total = 0
 // marks a failed compression.  One thread.
+// Progress for a host that copies finished parts while the kernel runs: every
+// lane's writes are made visible system-wide before lane 0 posts the word.
+__device__ __forceinline__ void post_progress(uint64_t* p, uint64_t v, uint32_t lane) {
+    __threadfence_system();
+    __syncwarp();
+    if (lane == 0) *reinterpret_cast<volatile uint64_t*>(p) = v;
+}
+
 template <int DT>
 __device__ void write_header(const CompressArgs& a, uint64_t total, uint32_t st) {
     const uint64_t n = a.n, C = a.num_chunks;
@@ -1007,6 +1019,7 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
             reinterpret_cast<uint64_t*>(a.out + kHeader)[c] = excl;
             reinterpret_cast<uint32_t*>(a.out + kHeader + 8 * uint64_t(C))[c] = len | (raw ? kRawFlag : 0u);
         }
+        if (a.progress && ok) post_progress(a.progress + 2 * uint64_t(c) + 1, (1ull << 63) | (excl + round16(len)), lane);
         __syncwarp();
         uint32_t prev = 0;
         if (lane == 0) {
@@ -1061,6 +1074,7 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
         else
             split_and_count<DT, SAMPLED ? 2 : 1>(cin, n_c, a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk, slot, regA,
                                           lane, pol_keep, pol_stream);
+        if (a.progress) post_progress(a.progress + 2 * uint64_t(c), 1, lane);
         uint32_t total = n_c;  // counts' total
         uint32_t cnt[8];
         reduce_hist(regA, lane, cnt);

@@ -44,6 +44,58 @@ bool host_mapped(const void* p, void** dev) {
 }
 }  // namespace
 
+namespace {
+// Copies one message's container to the host while its compression runs:
+// the remainder plane in runs of finished chunks (their split posted), the
+// exponent section in runs of placed chunks (their stream end posted), then,
+// once the kernel is done, the header and chunk table.  Progress words are
+// read from the host bank at prog_off (mapped memory the kernel writes).
+cudaError_t stream_out(int dtype, uint64_t n, const uint8_t* db, uint8_t* hb, uint64_t prog_off, cudaEvent_t done,
+                       cudaStream_t sx) {
+    using namespace uzip;
+    const uint64_t C = num_chunks(n);
+    const uint64_t rem_off = rem_offset(n), exp_off = exp_offset(dtype, n);
+    const uint64_t rem_end = rem_off + rem_plane_bytes(dtype, n);
+    const uint64_t rem_chunk = uint64_t(kChunk) / 8 * rem_bits(dtype);
+    const volatile uint64_t* prog = reinterpret_cast<const volatile uint64_t*>(hb + prog_off);
+    constexpr uint64_t kRun = 64;  // chunks per copy while the kernel runs
+    uint64_t rem_done = 0, exp_done = 0, exp_end = 0;
+    bool kernel_done = false;
+    cudaError_t err = cudaSuccess;
+    while (err == cudaSuccess) {
+        uint64_t p = rem_done;
+        while (p < C && prog[2 * p] != 0) ++p;
+        if (p > rem_done && (p - rem_done >= kRun || p == C || kernel_done)) {
+            const uint64_t lo = rem_off + rem_done * rem_chunk, hi = p == C ? rem_end : rem_off + p * rem_chunk;
+            err = cudaMemcpyAsync(hb + lo, db + lo, hi - lo, cudaMemcpyDeviceToHost, sx);
+            rem_done = p;
+        }
+        uint64_t q = exp_done, end = exp_end;
+        while (q < C) {
+            const uint64_t v = prog[2 * q + 1];
+            if (!(v >> 63)) break;
+            end = v & ~(1ull << 63);
+            ++q;
+        }
+        if (err == cudaSuccess && q > exp_done && (q - exp_done >= kRun || q == C || kernel_done)) {
+            if (end > exp_end)
+                err = cudaMemcpyAsync(hb + exp_off + exp_end, db + exp_off + exp_end, end - exp_end,
+                                      cudaMemcpyDeviceToHost, sx);
+            exp_done = q;
+            exp_end = end;
+        }
+        if ((rem_done == C && exp_done == C) || kernel_done) break;
+        const cudaError_t qs = cudaEventQuery(done);
+        if (qs == cudaSuccess) kernel_done = true;  // one more pass picks up the last posts
+        else if (qs != cudaErrorNotReady) err = qs;
+    }
+    if (err == cudaSuccess) err = cudaEventSynchronize(done);
+    // header, chunk table and padding, final once the kernel is done
+    if (err == cudaSuccess) err = cudaMemcpyAsync(hb, db, rem_off, cudaMemcpyDeviceToHost, sx);
+    return err;
+}
+}  // namespace
+
 extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d_msgs, const uint64_t* msg_elems,
                                           uint32_t n_msgs, void* const* d_bank, uint64_t bank_capacity,
                                           void* const* h_bank, uint64_t h_capacity, uint64_t* h_sizes,
@@ -51,7 +103,8 @@ extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d
     using namespace uzip;
     if (!valid_dtype(dtype)) return UZIP_ERR_UNSUPPORTED_DTYPE;
     if (n_msgs == 0 || !d_msgs || !msg_elems || !d_bank || !h_bank || !h_sizes) return UZIP_ERR_INVALID_ARG;
-    if (mode != UZIP_PIPE_EXACT && mode != UZIP_PIPE_BOUND && mode != UZIP_PIPE_SERIAL && mode != UZIP_PIPE_SIZED)
+    if (mode != UZIP_PIPE_EXACT && mode != UZIP_PIPE_BOUND && mode != UZIP_PIPE_SERIAL && mode != UZIP_PIPE_SIZED &&
+        mode != UZIP_PIPE_STREAMED)
         return UZIP_ERR_INVALID_ARG;
     uint64_t largest = 0;
     for (uint32_t k = 0; k < n_msgs; ++k) {
@@ -60,6 +113,9 @@ extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d
     }
     if (bank_capacity < uzip_max_compressed_size(dtype, largest)) return UZIP_ERR_CAPACITY;
     if (h_capacity < container_bound(dtype, largest)) return UZIP_ERR_CAPACITY;
+    // streamed: the host banks also hold 16 bytes of progress per chunk
+    const uint64_t prog_off = round16(container_bound(dtype, largest));
+    if (mode == UZIP_PIPE_STREAMED && h_capacity < prog_off + 16 * num_chunks(largest)) return UZIP_ERR_CAPACITY;
     void* h_dev[2] = {nullptr, nullptr};
     void* sizes_dev = nullptr;
     for (int b = 0; b < 2; ++b) {
@@ -87,16 +143,36 @@ extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d
             result = UZIP_ERR_CUDA;
             break;
         }
-        result = uzip_compress(d_msgs[k], dtype, msg_elems[k], d_bank[b], bank_capacity,
-                               static_cast<uint64_t*>(sizes_dev) + k, sc);
-        if (result != UZIP_OK) break;
+        if (mode == UZIP_PIPE_STREAMED) {
+            // progress words live past the container in the host bank
+            volatile uint64_t* prog = reinterpret_cast<volatile uint64_t*>(static_cast<uint8_t*>(h_bank[b]) + prog_off);
+            for (uint64_t i = 0; i < 2 * num_chunks(msg_elems[k]); ++i) prog[i] = 0;
+            if (msg_elems[k] > 0 && (!d_msgs[k] || (reinterpret_cast<uintptr_t>(d_msgs[k]) & 15))) {
+                result = UZIP_ERR_INVALID_ARG;
+                break;
+            }
+            uint64_t* prog_dev = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(h_dev[b]) + prog_off);
+            if (launch_compress(dtype, d_msgs[k], msg_elems[k], d_bank[b], static_cast<uint64_t*>(sizes_dev) + k, nullptr,
+                                0, sc, 0, prog_dev) != cudaSuccess) {
+                result = UZIP_ERR_CUDA;
+                break;
+            }
+        } else {
+            result = uzip_compress(d_msgs[k], dtype, msg_elems[k], d_bank[b], bank_capacity,
+                                   static_cast<uint64_t*>(sizes_dev) + k, sc);
+            if (result != UZIP_OK) break;
+        }
+        // streamed copies run while the kernel does: only they skip the wait
         if (!serial && (cudaEventRecord(compressed[b], sc) != cudaSuccess ||
-                        cudaStreamWaitEvent(sx, compressed[b], 0) != cudaSuccess)) {
+                        (mode != UZIP_PIPE_STREAMED && cudaStreamWaitEvent(sx, compressed[b], 0) != cudaSuccess))) {
             result = UZIP_ERR_CUDA;
             break;
         }
-        cudaError_t err;
-        if (mode == UZIP_PIPE_BOUND) {
+        cudaError_t err = cudaSuccess;
+        if (mode == UZIP_PIPE_STREAMED) {
+            err = stream_out(dtype, msg_elems[k], static_cast<const uint8_t*>(d_bank[b]),
+                             static_cast<uint8_t*>(h_bank[b]), prog_off, compressed[b], sx);
+        } else if (mode == UZIP_PIPE_BOUND) {
             err = cudaMemcpyAsync(h_bank[b], d_bank[b], container_bound(dtype, msg_elems[k]), cudaMemcpyDeviceToHost, sx);
         } else if (mode == UZIP_PIPE_SIZED) {
             // the size is known once this compression is done; message k-1's

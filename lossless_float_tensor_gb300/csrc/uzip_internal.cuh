@@ -251,11 +251,13 @@ cudaError_t launch_shape(const void* kern, int threads, size_t smem, int* sms, i
 // mode: 0 per-chunk choice, 1 whole message RAW, 2 gated (a one-warp kernel
 // decides from the first 64 KiB of input), 3 per-chunk choice with sampled
 // tables
+// progress (nullable, mapped host memory, 2 u64 per chunk): see CompressArgs
 cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
-                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s, int mode = 0);
+                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s, int mode = 0,
+                            uint64_t* progress = nullptr);
 cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                                          int32_t* d_status, uint32_t first_ticket, void* scratch_area, void* stash,
-                                         cudaStream_t s, int mode = 0);
+                                         cudaStream_t s, int mode = 0, uint64_t* progress = nullptr);
 
 // allocation-free compression: largest tensor and device count served by the
 // library's own work area

@@ -180,7 +180,7 @@ def test_query_size():
     assert total == oracle.compress(bits).size
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
 def test_pipeline_send(mode):
     import torch
 
@@ -192,13 +192,14 @@ def test_pipeline_send(mode):
     largest = max(m.size for m in msgs)
     cap = uz.uzip_max_compressed_size(0, largest)
     banks = [torch.empty(cap, dtype=torch.uint8, device="cuda") for _ in range(2)]
-    hb = [torch.zeros(cap, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    hcap = cap + 16 * (-(-largest // 65536))  # room for the streamed mode's progress words
+    hb = [torch.zeros(hcap, dtype=torch.uint8).pin_memory() for _ in range(2)]
     sizes = torch.zeros(len(msgs), dtype=torch.int64).pin_memory()
     s0 = torch.cuda.Stream()
     s1 = torch.cuda.Stream()
     torch.cuda.synchronize()
     st = uz.uzip_pipeline_send(0, [t.data_ptr() for t in d_msgs], [m.size for m in msgs],
-                               [b.data_ptr() for b in banks], cap, [h.data_ptr() for h in hb], cap,
+                               [b.data_ptr() for b in banks], cap, [h.data_ptr() for h in hb], hcap,
                                sizes.data_ptr(), mode, s0.cuda_stream, s1.cuda_stream)
     assert st == 0, uz.uzip_status_string(st)
     torch.cuda.synchronize()
