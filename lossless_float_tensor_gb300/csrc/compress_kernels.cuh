@@ -169,8 +169,11 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
 #pragma unroll
         for (int v = 0; v < int(PV); ++v) q[v] = ld_v4_hint(cin + (uint64_t(unit) * PV + v) * 16, pol_stream);
     };
-    // Batches of U units per lane, two batches in flight.
-    constexpr int U = es == 4 ? 2 : 4;
+    // Batches of U units per lane.  A unit's registers are refilled with the
+    // same unit of the next batch as soon as it has been processed, so the
+    // next batch's loads are in flight while this one is processed (one set
+    // of registers, one copy of the loop body).
+    constexpr int U = es == 4 ? 4 : 8;
     const uint32_t nb = nunits / (32 * U);
     const uint32_t head = nunits - nb * 32 * U;
     for (uint32_t u = lane; u < head; u += 32) {
@@ -178,21 +181,21 @@ __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, u
         load_unit(q, u);
         process(q, u);
     }
-    uint4 qa[U][PV], qb[U][PV];
+    uint4 qa[U][PV];
     auto unit_of = [&](uint32_t k, int u) -> uint32_t { return head + k * 32 * U + 32 * u + lane; };
     auto load = [&](uint4 (&q)[U][PV], uint32_t k) {
 #pragma unroll
         for (int u = 0; u < U; ++u) load_unit(q[u], unit_of(k, u));
     };
     if (nb > 0) load(qa, 0);
-    for (uint32_t k = 0; k < nb; k += 2) {
-        if (k + 1 < nb) load(qb, k + 1);
+#pragma unroll 1
+    for (uint32_t k = 0; k < nb; ++k) {
+        const bool more = k + 1 < nb;
 #pragma unroll
-        for (int u = 0; u < U; ++u) process(qa[u], unit_of(k, u));
-        if (k + 1 >= nb) break;
-        if (k + 2 < nb) load(qa, k + 2);
-#pragma unroll
-        for (int u = 0; u < U; ++u) process(qb[u], unit_of(k + 1, u));
+        for (int u = 0; u < U; ++u) {
+            process(qa[u], unit_of(k, u));
+            if (more) load_unit(qa[u], unit_of(k + 1, u));
+        }
     }
     // ragged tail (n_c not a multiple of 16): element by element
     for (uint32_t i = nunits * 16 + lane; i < n_c; i += 32) {
@@ -281,7 +284,7 @@ __device__ void split_and_count_packed(const uint8_t* __restrict__ cin, uint32_t
 #pragma unroll
         for (int v = 0; v < int(PV); ++v) q[v] = ld_v4_hint(cin + (uint64_t(unit) * PV + v) * 16, pol_stream);
     };
-    // batches of U units per lane, two batches in flight
+    // batches of U units per lane, refilled unit by unit as above
     constexpr int U = es == 2 ? 2 : 4;
     const uint32_t nb = nunits / (32 * U);
     const uint32_t head = nunits - nb * 32 * U;
@@ -290,21 +293,21 @@ __device__ void split_and_count_packed(const uint8_t* __restrict__ cin, uint32_t
         load_unit(q, u);
         process(q, u);
     }
-    uint4 qa[U][PV], qb[U][PV];
+    uint4 qa[U][PV];
     auto unit_of = [&](uint32_t k, int u) -> uint32_t { return head + k * 32 * U + 32 * u + lane; };
     auto load = [&](uint4 (&q)[U][PV], uint32_t k) {
 #pragma unroll
         for (int u = 0; u < U; ++u) load_unit(q[u], unit_of(k, u));
     };
     if (nb > 0) load(qa, 0);
-    for (uint32_t k = 0; k < nb; k += 2) {
-        if (k + 1 < nb) load(qb, k + 1);
+#pragma unroll 1
+    for (uint32_t k = 0; k < nb; ++k) {
+        const bool more = k + 1 < nb;
 #pragma unroll
-        for (int u = 0; u < U; ++u) process(qa[u], unit_of(k, u));
-        if (k + 1 >= nb) break;
-        if (k + 2 < nb) load(qa, k + 2);
-#pragma unroll
-        for (int u = 0; u < U; ++u) process(qb[u], unit_of(k + 1, u));
+        for (int u = 0; u < U; ++u) {
+            process(qa[u], unit_of(k, u));
+            if (more) load_unit(qa[u], unit_of(k + 1, u));
+        }
     }
     // ragged tail (fewer than 32 values): its fields start byte aligned
     // (32 W bits per unit); lane 0 packs them, the lanes count and copy the
@@ -670,7 +673,7 @@ inline __device__ bool encode_slot(uint8_t* slot, uint32_t n_c, uint32_t table_s
         st.x = active ? xn : st.x;
     }
     if (T0 == 0) return true;
-    uint32_t va[32], vb[32];
+    uint32_t va[32];
     auto load_ex = [&](uint32_t (&v)[32], int32_t t) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = ld_slot_u8(slot + (uint32_t(t - j) * 32 + lane));
@@ -694,11 +697,14 @@ inline __device__ bool encode_slot(uint8_t* slot, uint32_t n_c, uint32_t table_s
     // the bytes of steps above t0 + 32 qualify: u16 index 16 (t0 + 33) and up.
     // Loads of later steps are in flight or not yet issued, and nothing orders
     // them against another lane's store.
-    auto run_block = [&](const uint32_t (&v)[32], int32_t t0) -> bool {
+    auto run_block = [&](uint32_t (&v)[32], int32_t t0, bool load_next) -> bool {
         if (st.pos - 32 * 32 < 16 * (t0 + 33)) return false;
+        // byte of step t0 - 32 - j (the next block) at nxt - 32 j
+        const uint8_t* nxt = slot + (uint32_t(load_next ? t0 - 32 : 0) * 32 + lane);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const uint4 e = lds_table(table_s + 8 * v[j]);
+            if (load_next) v[j] = ld_slot_u8(nxt - 32 * j);
             const bool emit = st.x > e.z;
             const uint32_t b = __ballot_sync(0xFFFFFFFFu, emit);
             const uint32_t w = st.x;
@@ -709,21 +715,18 @@ inline __device__ bool encode_slot(uint8_t* slot, uint32_t n_c, uint32_t table_s
         }
         return true;
     };
-    // whole blocks from step T0 - 1 down, two per iteration (the buffers
-    // alternate); an odd count ends with a single block
+    // whole blocks from step T0 - 1 down.  Once step j of a block has read
+    // its table entry, v[j] is refilled with the exponent byte of step j of
+    // the next block, so that block's loads run during this one (one set of
+    // 32 registers, one copy of the block's code).
     load_ex(va, T0 - 1);
     prefetch_block(T0 - 65);
-    for (int32_t t0 = T0 - 1;; t0 -= 64) {
-        const bool has_b = t0 >= 63;
-        if (has_b) load_ex(vb, t0 - 32);
+#pragma unroll 1
+    for (int32_t t0 = T0 - 1;; t0 -= 32) {
+        const bool has_next = t0 >= 63;
         prefetch_block(t0 - 96);
-        if (!run_block(va, t0)) return false;
-        if (!has_b) break;
-        const bool more = t0 >= 95;
-        if (more) load_ex(va, t0 - 64);
-        prefetch_block(t0 - 128);
-        if (!run_block(vb, t0 - 32)) return false;
-        if (!more) break;
+        if (!run_block(va, t0, has_next)) return false;
+        if (!has_next) break;
     }
     flush_one(w2, e2, b2);
     flush_one(w1, e1, b1);
