@@ -484,7 +484,7 @@ __device__ void normalise(const uint32_t c[8], uint32_t n_c, uint32_t lane, uint
 // division magic of every frequency, built at compile time
 __device__ const MagicTable g_magic = make_magic_table();
 
-// encode table row for each present symbol: {m, add} and {(f << 20) - 1, (M - f) | cum << 12 | sh << 27}
+// encode table row for each present symbol: {m, add} and {(f << 20) - 1, sh | cum << 5 | (M - f) << 20}
 inline __device__ void build_enc_table(const Norm& nm, uint32_t lane, uint8_t* table, uint8_t* regB) {
     uint32_t lsum = 0;
 #pragma unroll
@@ -514,7 +514,7 @@ inline __device__ void build_enc_table(const Norm& nm, uint32_t lane, uint8_t* t
         e.x = dm.m;
         e.y = dm.add;
         e.z = uint32_t((uint64_t(f) << 20) - 1);
-        e.w = (kM - f) | (cums[s] << 12) | (dm.sh << 27);
+        e.w = dm.sh | (cums[s] << 5) | ((kM - f) << 20);
         *reinterpret_cast<uint2*>(table + 8 * s) = make_uint2(e.x, e.y);
         *reinterpret_cast<uint2*>(table + 2048 + 8 * s) = make_uint2(e.z, e.w);
     }
@@ -523,7 +523,9 @@ inline __device__ void build_enc_table(const Norm& nm, uint32_t lane, uint8_t* t
 
 // ---------------------------------------------------------------------------
 // rANS encode (rule R6).  The table entry of a symbol is
-// {m, add, (f << 20) - 1, (M - f) | cum << 12 | sh << 27}.
+// {m, add, (f << 20) - 1, sh | cum << 5 | (M - f) << 20}: sh sits in the
+// low 5 bits so that a wrapping funnel shift by the packed word shifts by sh,
+// and M - f in the top 12 bits comes out with one shift.
 
 // Table loads are written as side-effect-free asm: the table does not change
 // while a chunk is encoded, so the compiler may issue them as early as it likes
@@ -548,11 +550,10 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 
 __device__ __forceinline__ uint32_t rans_update(uint32_t x, const uint4 e, bool emit) {
     const uint32_t xr = emit ? (x >> 16) : x;
-    const uint32_t sh = e.w >> 27;
     const uint64_t t = uint64_t(xr) * e.x + e.y;
-    const uint32_t q = uint32_t(t >> 32) >> sh;
-    const uint32_t mmf = e.w & 0xFFFu;
-    const uint32_t cum = (e.w >> 12) & 0xFFFu;
+    const uint32_t q = __funnelshift_r(uint32_t(t >> 32), 0u, e.w);  // shift by e.w mod 32 = sh
+    const uint32_t mmf = e.w >> 20;
+    const uint32_t cum = (e.w >> 5) & 0xFFFu;
     return q * mmf + (xr + cum);
 }
 
