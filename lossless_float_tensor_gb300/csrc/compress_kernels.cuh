@@ -1264,6 +1264,11 @@ cudaError_t launch_mode(CompressArgs a, int mode, bool stash, cudaStream_t s) {
     if (grid > work) grid = work;
     if (stash && grid > stash_warps(n)) grid = stash_warps(n);  // two slots per warp
     if (grid < 1) grid = 1;
+    // As few warps as give the same number of rounds of chunks, so that the
+    // last round is (nearly) full: 8192 chunks take 7 rounds of 1171 warps
+    // rather than 6.7 of 1216.
+    const uint64_t rounds = (work + grid - 1) / grid;  // work >= 1, grid >= 1
+    grid = (work + rounds - 1) / rounds;
     kern<<<dim3(uint32_t(grid)), dim3(32), kCompressSmem, s>>>(a);
     return cudaGetLastError();
 }
