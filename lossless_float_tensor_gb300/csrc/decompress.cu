@@ -232,8 +232,9 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
     // the loop.  The state update f (x >> 12) + (x mod 4096) - cum is computed
     // as (x >> 12)(f - 4096) + x - cum (exact modulo 2^32, and the result is
     // below 2^32), so one table entry {f - 4096, -cum} feeds it directly.
-    // `cur` advances by scale words per consumed word (the ring path keeps
-    // a per-lane byte cursor, the others the word position).
+    // `cur` advances by scale words per consumed word.  This form serves
+    // partial chunks and streams read from global memory; full chunks staged
+    // in the shared-memory ring take rstep below, which saves the shuffle.
     auto step = [&](uint32_t t, uint32_t r, bool active, uint32_t win, uint32_t& cur, uint32_t scale) {
         const uint32_t slot = x & (kM - 1);
         uint32_t s, g, nc;
@@ -306,13 +307,11 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
         uint4 pend = make_uint4(0, 0, 0, 0);
         uint32_t pend_piece = 0;
         bool has_pend = false;
-        // per-lane byte cursor: offset in the record of word pos + lane
-        const uint32_t lane_off = wb0 + 2 * lane;
-        uint32_t rq = lane_off;
+        uint32_t rq = wb0;  // byte offset in the record of word pos (the same in every lane)
         auto top_up = [&]() {
             if (has_pend) store_piece(pend_piece, pend);
             has_pend = false;
-            pos = (rq - lane_off) >> 1;
+            pos = (rq - wb0) >> 1;
             const uint32_t cur = (wb0 + 2 * pos) >> 8;
             uint32_t need_end = ((wb0 + 2 * (pos + 8 * 32)) >> 8) + 1;
             need_end = need_end < npieces ? need_end : npieces;
@@ -328,10 +327,27 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
                 ++next_piece;
             }
         };
-        auto rwin = [&]() -> uint32_t {
-            uint32_t v;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(ring_s + (rq & 1023u)) : "memory");
-            return v;
+        // A ring step: a renormalising lane reads its word straight from the
+        // ring, at pos plus its rank among the renormalising lanes (one
+        // shared load on the state's chain instead of a window load plus a
+        // shuffle; the ring holds words pos .. pos + 31 at every step).
+        auto rstep = [&](uint32_t t, uint32_t r) {
+            const uint32_t slot = x & (kM - 1);
+            uint32_t s, g, nc;
+            asm("ld.shared.u8 %0, [%1];" : "=r"(s) : "r"(slot_s + slot));
+            asm("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(g), "=r"(nc) : "r"(gc_s + 8 * s));
+            const uint32_t xn = (x >> kProbBits) * g + x + nc;
+            const bool need = xn < kRansL;
+            const uint32_t b = __ballot_sync(0xFFFFFFFFu, need);
+            uint32_t w;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=r"(w) : "r"(ring_s + ((rq + 2 * __popc(b & lt)) & 1023u)) : "memory");
+            rq += 2 * __popc(b);
+            x = need ? ((xn << 16) | w) : xn;
+            const uint32_t v = merge_fast<DT>(s, r);
+            const uint64_t i = 32 * uint64_t(t) + lane;
+            if (es == 2) reinterpret_cast<uint16_t*>(out)[i] = uint16_t(v);
+            else if (es == 4) reinterpret_cast<uint32_t*>(out)[i] = v;
+            else out[i] = uint8_t(v);
         };
         // Both streams are cold in L2 when decompression starts: pull the
         // remainder bytes of the steps 64 ahead and the stream bytes ~1 KiB
@@ -342,7 +358,7 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
             if (lane < kRemLines && t_ahead + 16 <= kSteps)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(rem + uint64_t(t_ahead) * kRemStep + 128 * lane));
             if (lane >= 30) {
-                const uint32_t at = (rq - 2 * lane) + 1024 + 128 * (lane - 30);
+                const uint32_t at = rq + 1024 + 128 * (lane - 30);
                 if (at < nlines * 16) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + at));
             }
         };
@@ -359,16 +375,16 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
             for (int j = 0; j < PF; ++j) rbk[j] = load_rem_full(t0 + PF + j);
             top_up();
 #pragma unroll
-            for (int j = 0; j < PF; ++j) step(t0 + j, ra[j], true, rwin(), rq, 2);
+            for (int j = 0; j < PF; ++j) rstep(t0 + j, ra[j]);
             if (t0 + 2 * PF < kSteps) {
 #pragma unroll
                 for (int j = 0; j < PF; ++j) ra[j] = load_rem_full(t0 + 2 * PF + j);
             }
             top_up();
 #pragma unroll
-            for (int j = 0; j < PF; ++j) step(t0 + PF + j, rbk[j], true, rwin(), rq, 2);
+            for (int j = 0; j < PF; ++j) rstep(t0 + PF + j, rbk[j]);
         }
-        pos = (rq - lane_off) >> 1;
+        pos = (rq - wb0) >> 1;
     } else if (n_c == kChunk) {
         // The word stream is read sequentially, ~11 bytes per step: pull the
         // lines about 40 steps ahead into L1 so a step never waits on a first
