@@ -35,6 +35,25 @@ def test_edge_sizes(n, dtype):
     _parity(bits)
 
 
+@pytest.mark.parametrize("chunks", [1217, 2433])
+def test_chunk_counts_past_a_full_grid(chunks):
+    """Chunk counts one past a whole number of compressor rounds (8 warps per
+    SM on 152 SMs) and a ragged tail: the trimmed grids still cover every
+    chunk once, and the container is the oracle's."""
+    _parity(synth.normal_bf16(chunks * 65536 - 77, 0.02, 14, chunks))
+
+
+def test_decoder_two_rounds_with_ragged_tail():
+    """More chunks than the decoder's resident warps (28 per SM on 152 SMs):
+    the trimmed grid decodes every chunk of a compressed tensor exactly."""
+    n = 4257 * 65536 + 5
+    bits = synth.normal_bf16(n, 0.02, 15, 0)
+    comp, status = gu.gpu_compress(bits)
+    assert status == 0
+    back, st = gu.gpu_decompress(comp, gu.dtype_of(bits), n)
+    assert st == 0 and np.array_equal(back, bits)
+
+
 def test_c1_full():
     comp = _parity(synth.c1())
     assert abs(comp.size / (2 << 20) - 0.661) < 0.01
