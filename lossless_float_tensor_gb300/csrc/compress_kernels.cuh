@@ -91,8 +91,7 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t lane, ui
 // of the chunk (a sampled table), 0 none (a whole-message RAW container).
 template <int DT, int CM = 1>
 __device__ void split_and_count(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* __restrict__ rem_dst,
-                                uint8_t* __restrict__ ex_dst, uint8_t* hist, uint32_t lane, uint64_t pol_keep,
-                                uint64_t pol_stream) {
+                                uint8_t* __restrict__ ex_dst, uint8_t* hist, uint32_t lane, uint64_t pol_stream) {
     if constexpr (CM != 0) {
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll 8
@@ -1006,7 +1005,6 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
     const uint64_t rem_off = rem_offset(n);
     const uint64_t exp_off = exp_offset(DT, n);
     constexpr uint32_t es = Traits<DT>::kEs;
-    const uint64_t pol_keep = policy_evict_last();
     const uint64_t pol_stream = policy_evict_first();
     const uint32_t processed = C - a.first_ticket;
     const uint32_t table_s = smem_addr(regA);
@@ -1077,7 +1075,7 @@ __global__ void __launch_bounds__(32) compress_kernel(CompressArgs a) {
                                                  regA, lane, pol_stream);
         else
             split_and_count<DT, SAMPLED ? 2 : 1>(cin, n_c, a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk, slot, regA,
-                                          lane, pol_keep, pol_stream);
+                                          lane, pol_stream);
         if (a.progress) post_progress(a.progress + 2 * uint64_t(c), 1, lane);
         uint32_t total = n_c;  // counts' total
         uint32_t cnt[8];
@@ -1181,7 +1179,7 @@ __global__ void __launch_bounds__(32) gate_kernel(CompressArgs a, uint32_t n_s) 
     if constexpr (Fmt<DT>::kPacked)
         split_and_count_packed<DT>(a.in, n_s, rem, slot, regA, lane, pol);
     else
-        split_and_count<DT>(a.in, n_s, rem, slot, regA, lane, pol, pol);
+        split_and_count<DT>(a.in, n_s, rem, slot, regA, lane, pol);
     uint32_t cnt[8];
     reduce_hist(regA, lane, cnt);
     __syncwarp();
@@ -1220,8 +1218,7 @@ __global__ void __launch_bounds__(32) raw_kernel(CompressArgs a) {
             split_and_count_packed<DT, 0>(cin, n_c, a.out + rem_off + c * Fmt<DT>::kRemChunk, dst, nullptr, lane,
                                               pol);
         else
-            split_and_count<DT, 0>(cin, n_c, a.out + rem_off + c * Fmt<DT>::kRemChunk, dst, nullptr, lane, pol,
-                                       pol);
+            split_and_count<DT, 0>(cin, n_c, a.out + rem_off + c * Fmt<DT>::kRemChunk, dst, nullptr, lane, pol);
         for (uint32_t i = n_c + lane; i < round16(n_c); i += 32) dst[i] = 0;
         if (lane == 0) {
             reinterpret_cast<uint64_t*>(a.out + kHeader)[c] = c * kChunk;

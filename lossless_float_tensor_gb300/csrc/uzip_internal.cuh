@@ -133,11 +133,6 @@ constexpr uint32_t kDecList = 1024;         // present symbols, u32[256]: cum <<
 constexpr uint32_t kDecWarpSmem = kDecSlotTable + kDecSymTable + kDecList;
 
 // ---- inline PTX helpers ----------------------------------------------------
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
