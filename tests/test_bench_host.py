@@ -1,0 +1,44 @@
+"""Host-side helpers of the benchmark (no GPU): the DRAM traffic figure is
+taken from the committed ncu summary only while the kernel sources are the
+ones it was captured on, and the replica throughput counts every rank."""
+import json
+import os
+
+import pytest
+
+import bench
+
+
+def _committed():
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as fh:
+        return json.load(fh)
+
+
+def test_kernel_hash_is_stable_hex():
+    h = bench.kernel_hash()
+    assert h == bench.kernel_hash()
+    assert len(h) == 16 and int(h, 16) >= 0
+
+
+@pytest.mark.parametrize("kernel", ["compress", "decompress"])
+def test_traffic_only_for_the_captured_sources(kernel, monkeypatch):
+    entry = _committed()[kernel]
+    monkeypatch.setattr(bench, "kernel_hash", lambda: entry["source_hash"])
+    got = bench.profiled_traffic(kernel)
+    assert got == entry["dram_bytes_per_launch_full"]
+    # scaled from the capture by the chunk counts of the two launches
+    small = entry["dram_bytes_read_small"] + entry["dram_bytes_write_small"]
+    chunks = lambda n: -(-n // 65536)  # noqa: E731
+    assert got == pytest.approx(small * chunks(entry["elements_full"]) / chunks(entry["elements_small"]))
+    monkeypatch.setattr(bench, "kernel_hash", lambda: "0" * 16)
+    assert bench.profiled_traffic(kernel) is None
+
+
+def test_unknown_kernel_has_no_traffic():
+    assert bench.profiled_traffic("no_such_kernel") is None
+
+
+def test_replica_throughput_sums_ranks():
+    one = bench.replica_throughput_gbs(1 << 30, 10, 5.0, 1)
+    assert one == pytest.approx((1 << 30) * 10 / 5e-3 / 1e9)
+    assert bench.replica_throughput_gbs(1 << 30, 10, 5.0, 4) == pytest.approx(4 * one)
