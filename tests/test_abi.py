@@ -101,3 +101,17 @@ def test_host_argument_checks(uz):
     assert uz.uzip_decompress(None, 1 << 20, fake, 0, 10, None, 0) == uz.UZIP_ERR_INVALID_ARG
     assert uz.uzip_decompress(fake, 1 << 20, fake, 5, 10, None, 0) == uz.UZIP_ERR_UNSUPPORTED_DTYPE
     assert uz.uzip_query_size(None, 0)[0] == uz.UZIP_ERR_INVALID_ARG
+
+
+def test_package_refuses_to_import_without_the_library(monkeypatch):
+    """No CPU fallback: with the shared library absent, importing the binding
+    fails loudly instead of degrading."""
+    import importlib.util
+
+    path = os.path.join(ROOT, "lossless_float_tensor_gb300", "__init__.py")
+    real_exists = os.path.exists
+    monkeypatch.setattr(os.path, "exists", lambda p: False if str(p).endswith("libuzip.so") else real_exists(p))
+    spec = importlib.util.spec_from_file_location("_uzip_without_library", path)
+    mod = importlib.util.module_from_spec(spec)
+    with pytest.raises(ImportError, match="not built"):
+        spec.loader.exec_module(mod)
