@@ -151,6 +151,154 @@ def replica_throughput_gbs(bytes_per_rank: int, steps: int, max_ms: float, world
     return world * bytes_per_rank * steps / (max_ms / 1e3) / 1e9
 
 
+def host_description():
+    """Host cores and CPU model (x86: 'model name'; Arm: implementer/part)."""
+    model, impl, part = None, None, None
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                k, _, v = line.partition(":")
+                k, v = k.strip(), v.strip()
+                if k == "model name" and model is None:
+                    model = v
+                elif k == "CPU implementer" and impl is None:
+                    impl = v
+                elif k == "CPU part" and part is None:
+                    part = v
+    except OSError:
+        pass
+    if model is None and impl is not None:
+        model = f"Arm CPU implementer {impl}, part {part}"
+    return {"host_cores": os.cpu_count(), "cpu_model": model or "unknown"}
+
+
+def config_inputs(name):
+    """(dtype code, list of bit arrays) of one workload of the per-config table."""
+    import synth
+
+    if name == "c1":
+        return 0, [synth.c1()]
+    if name == "c2":
+        return 0, [synth.c2_tensor(t) for t in range(7)]
+    if name == "c3":
+        return 1, [synth.c3()]
+    if name == "c4":
+        return 0, [synth.c4()]
+    if name == "c5m0":
+        return 0, [synth.c5_message(0)]
+    raise ValueError(name)
+
+
+def oracle_job(name):
+    """One single-threaded oracle run (compress, then decompress) over a whole
+    workload of the per-config table, in a process of its own; returns the
+    timings and a hash of each container (compared with the GPU's)."""
+    import hashlib
+
+    import numpy as np
+
+    import oracle
+
+    dtype, arrays = config_inputs(name)
+    t_c = t_d = 0.0
+    hashes, total, nbytes = [], 0, 0
+    for bits in arrays:
+        t0 = time.perf_counter()
+        c = oracle.compress(bits, dtype)
+        t1 = time.perf_counter()
+        back = oracle.decompress(c, dtype, bits.size)
+        t2 = time.perf_counter()
+        assert np.array_equal(back.view(bits.dtype), bits)
+        t_c += t1 - t0
+        t_d += t2 - t1
+        hashes.append(hashlib.sha256(c.tobytes()).hexdigest())
+        total += c.size
+        nbytes += bits.nbytes
+    return {"config": name, "input_bytes": nbytes, "compressed_bytes": total, "compress_s": t_c, "decompress_s": t_d,
+            "compress_gbs": nbytes / t_c / 1e9, "decompress_gbs": nbytes / t_d / 1e9, "sha256": hashes}
+
+
+def start_oracle_jobs(names):
+    """Oracle runs in spawned processes (1 thread each), started before the
+    GPU work so they overlap it."""
+    import multiprocessing as mp
+
+    ctx = mp.get_context("spawn")
+    pool = ctx.Pool(processes=max(1, min(len(names), (os.cpu_count() or 2) - 1)))
+    return pool, {n: pool.apply_async(oracle_job, (n,)) for n in names}
+
+
+CONFIG_LABELS = {
+    "c1": "1,048,576 bf16 ~ N(0, 0.02); L2-resident (2 MiB), no flush",
+    "c2": "Llama-3-8B-shaped layer, 7 bf16 weight tensors (218,103,808 values), one call each, summed; L2 flushed",
+    "c3": "268,435,456 fp32 gradients with specials (1 GiB)",
+    "c4": "[8, 8192, 8192] bf16 activations, 0.5*t(4), outliers x50, one random chunk (1 GiB)",
+    "c5m0": "c5 message 0: first 1 GiB of the Llama-3-8B-shaped parameter set, bf16 ~ N(0, 0.02)",
+}
+
+
+def measure_config(name, dtype, arrays, dev, peak, flush_l2):
+    """GPU compress / decompress of every tensor of a workload: CUDA events,
+    mean of 5 launches after 3 warm-ups (L2 flushed before each timed launch
+    when the inputs are smaller than L2), summed over the tensors; plus the
+    container hashes and a bit-exact round-trip check."""
+    import hashlib
+
+    import numpy as np
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+
+    stream = torch.cuda.Stream(dev)
+    sp = stream.cuda_stream
+    scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush_l2 else None
+    tc = td = 0.0
+    nbytes = total = 0
+    hashes, exact = [], True
+    for bits in arrays:
+        x = torch.from_numpy(np.ascontiguousarray(bits).view(np.uint8)).to(dev)
+        n = bits.size
+        cap = uz.uzip_max_compressed_size(dtype, n)
+        comp = torch.empty(cap, dtype=torch.uint8, device=dev)
+        size = torch.zeros((), dtype=torch.int64, device=dev)
+        out = torch.empty_like(x)
+        status = torch.zeros((), dtype=torch.int32, device=dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(5)]
+        with torch.cuda.stream(stream):
+            for k in range(8):
+                e = ev[k - 3] if k >= 3 else None
+                if e and scrub is not None:
+                    scrub.fill_(k)
+                if e:
+                    e[0].record(stream)
+                st = uz.uzip_compress(x.data_ptr(), dtype, n, comp.data_ptr(), cap, size.data_ptr(), sp)
+                if e:
+                    e[1].record(stream)
+                    if scrub is not None:
+                        scrub.fill_(k + 1)
+                    e[2].record(stream)
+                st2 = uz.uzip_decompress(comp.data_ptr(), cap, out.data_ptr(), dtype, n, status.data_ptr(), sp)
+                if e:
+                    e[3].record(stream)
+                if st or st2:
+                    raise RuntimeError(f"{name}: uzip status {st} {st2}")
+        torch.cuda.synchronize(dev)
+        tot = int(size.item())
+        exact = exact and int(status.item()) == 0 and torch.equal(out, x)
+        hashes.append(hashlib.sha256(comp[:tot].cpu().numpy().tobytes()).hexdigest())
+        tc += statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+        td += statistics.mean(e[2].elapsed_time(e[3]) for e in ev) / 1e3
+        nbytes += bits.nbytes
+        total += tot
+        del x, comp, out
+    moved = nbytes + total
+    return {"config": name, "workload": CONFIG_LABELS[name], "input_bytes": nbytes, "compressed_bytes": total,
+            "ratio": total / nbytes, "compress_ms": tc * 1e3, "decompress_ms": td * 1e3,
+            "compress_gbs": nbytes / tc / 1e9, "decompress_gbs": nbytes / td / 1e9,
+            "compress_frac": moved / tc / 1e9 / peak, "decompress_frac": moved / td / 1e9 / peak,
+            "round_trip_exact": bool(exact), "sha256": hashes}
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -158,6 +306,12 @@ def run_ours(args, rank, world, local_rank):
     import lossless_float_tensor_gb300 as uz
     import synth
 
+    # the oracle's single-threaded runs over whole workloads, in spawned
+    # processes overlapping the GPU work (rank 0, default sizes only)
+    oracle_pool, oracle_runs = None, {}
+    if rank == 0 and not args.no_cpu_baseline and args.elements is None:
+        names = ["c4"] if args.no_configs else ["c4", "c1", "c2", "c3", "c5m0"]
+        oracle_pool, oracle_runs = start_oracle_jobs(names)
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     bits = synth.c4(n=args.elements)
@@ -231,10 +385,43 @@ def run_ours(args, rank, world, local_rank):
               "kernel": "decompress_kernel<bf16>", "algorithmic_bytes_per_launch": dec_bytes, "ms_per_launch": md,
               "peak_source": f"{peak_kind} hbm_gbs"}
     dominant = roof_c if mc >= md else roof_d
-    cpu = None if args.no_cpu_baseline else cpu_baseline(bits)
-    pipe = None if args.no_pipeline else run_pipeline(args, dev)
+    c5_msgs = None
+    pipe = None
+    if not args.no_pipeline and args.elements is None:
+        pipe, c5_msgs = run_pipeline(args, dev)
+    configs = None
+    if not args.no_configs and args.elements is None:
+        configs = run_configs(args, dev, peak, x, bits, c5_msgs)
+    del c5_msgs
+    torch.cuda.empty_cache()
     sweep = None if args.no_dtypes else run_dtype_sweep(args, dev, peak)
     gate = None if args.no_gate else run_gate(args, dev, x, n, peak)
+    cpu = None
+    if oracle_pool is not None:
+        results = {k: r.get() for k, r in oracle_runs.items()}
+        oracle_pool.close()
+        oracle_pool.join()
+        c4r = results["c4"]
+        cpu = {"value": 2 * c4r["input_bytes"] / (c4r["compress_s"] + c4r["decompress_s"]) / 1e9, "unit": "GB/s",
+               "cores": 1, "kind": "oracle",
+               "sample": "the whole workload (536,870,912 values), compress "
+                         f"{c4r['compress_s']:.1f} s + decompress {c4r['decompress_s']:.1f} s, one thread",
+               "compress_gbs": c4r["compress_gbs"], "decompress_gbs": c4r["decompress_gbs"], **host_description()}
+        if configs is not None:
+            for row in configs["rows"]:
+                r = results.get(row["config"])
+                if r is not None:
+                    row["oracle_compress_gbs"] = r["compress_gbs"]
+                    row["oracle_decompress_gbs"] = r["decompress_gbs"]
+                    row["oracle_bytes_equal"] = r["sha256"] == row["sha256"]
+            configs["oracle"] = {"cores": 1, "kind": "oracle, single-threaded C, one process per config",
+                                 **host_description()}
+        # the headline tensor's container against the oracle's
+        c4_gpu = hashlib.sha256(comp[:total].cpu().numpy().tobytes()).hexdigest()
+        cpu["oracle_bytes_equal"] = c4r["sha256"] == [c4_gpu]
+    if configs is not None:
+        for row in configs["rows"]:
+            row["sha256"] = [h[:16] for h in row["sha256"]]
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -246,10 +433,29 @@ def run_ours(args, rank, world, local_rank):
         "ratio": total / in_bytes, "compressed_bytes": total,
         "roofline": dominant, "roofline_compress": roof_c, "roofline_decompress": roof_d,
         "clocks": clk.summary(), "e2e": e2e, "gpu_launches": 2 * args.steps,
-        "wall_s_timed_region": wall, "cpu_baseline": cpu, "pipeline": pipe, "dtype_sweep": sweep, "gate": gate,
-        "kernel_source_hash": kernel_hash(),
+        "wall_s_timed_region": wall, "cpu_baseline": cpu, "configs": configs, "pipeline": pipe,
+        "dtype_sweep": sweep, "gate": gate, "kernel_source_hash": kernel_hash(),
     }
     return line
+
+
+def run_configs(args, dev, peak, x4, bits4, c5_msgs):
+    """The per-config table: GPU compress / decompress GB/s, ratio and
+    fraction of the HBM roofline for c1 (L2-resident), c2 (seven tensors, one
+    call each), c3 (fp32), c4 and the first c5 message, with a hash of every
+    container (compared with the oracle's when its runs are done)."""
+    import numpy as np
+
+    rows = []
+    for name in ["c1", "c2", "c3"]:
+        dtype, arrays = config_inputs(name)
+        rows.append(measure_config(name, dtype, arrays, dev, peak, flush_l2=name == "c2"))
+        del arrays
+    rows.append(measure_config("c4", 0, [bits4], dev, peak, flush_l2=False))
+    if c5_msgs is not None:
+        m0 = c5_msgs[0].cpu().numpy().view(np.uint16)
+        rows.append(measure_config("c5m0", 0, [m0], dev, peak, flush_l2=False))
+    return {"unit": "GB/s of input bytes; fractions of the measured HBM copy bandwidth", "rows": rows}
 
 
 def run_e2e(args, x, bits, comp, cap, size, out, status, stream, dev, total):
@@ -300,69 +506,85 @@ def run_e2e(args, x, bits, comp, cap, size, out, status, stream, dev, total):
 
 
 def run_pipeline(args, dev):
-    """Split-send pipeline (two streams, two ping-pong banks) on c5-shaped
-    messages: the first 1 GiB message of the Llama-3-8B-shaped parameter set
-    (bf16 ~ N(0, 0.02)) is sent `reps` times, and prefixes of it give the
-    64 KiB .. 1 GiB size sweep.  Reported: input GB/s of the pipelined modes
-    (exact-size copy kernel into mapped pinned memory; exact-size
-    cudaMemcpyAsync issued once the host has read the size; streamed copies of
-    finished remainder and stream runs while the message compresses;
-    bound-size cudaMemcpyAsync), of compress-then-copy on one stream (no
-    overlap), and of a plain device-to-host copy of the uncompressed bytes.
-    Also the latency of one 1 GiB message: from the call to the last byte on
-    the host, sized versus streamed."""
+    """Split-send pipeline (two streams, two device banks, two pinned host
+    banks) over the whole c5 workload: the 15 messages of the 8,030,261,248
+    bf16 Llama-3-8B-shaped parameter set (16.06 GB) go through each mode in
+    one call, against a plain device-to-host copy of the same bytes; then a
+    message-size sweep (64 KiB .. 1 GiB, prefixes of message 0) with the
+    default threshold under which a message travels as a whole-message RAW
+    container.  Modes: exact-size copy kernel into mapped pinned memory;
+    exact-size cudaMemcpyAsync once the host has read the size; streamed copies
+    of finished remainder and stream runs while the message compresses;
+    bound-size cudaMemcpyAsync; compress-then-copy on one stream (no overlap).
+    Host wall clock including the final synchronisation.  Returns the figures
+    and the device copies of the messages."""
     import numpy as np
     import torch
 
     import lossless_float_tensor_gb300 as uz
     import synth
 
-    msg = synth.c5_message(0)
-    n_max = msg.size
-    x = torch.from_numpy(msg.view(np.int16)).to(dev)
+    sizes = synth.c5_message_sizes()
+    t_gen = time.perf_counter()
+    msgs = [torch.from_numpy(synth.c5_message(k).view(np.int16)).to(dev) for k in range(len(sizes))]
+    t_gen = time.perf_counter() - t_gen
+    n_max = max(sizes)
     cap = uz.uzip_max_compressed_size(uz.UZIP_BF16, n_max)
     banks = [torch.empty(cap, dtype=torch.uint8, device=dev) for _ in range(2)]
     hcap = cap + 16 * (-(-n_max // 65536))  # the streamed mode keeps progress words past the container
     hb = [torch.empty(hcap, dtype=torch.uint8).pin_memory() for _ in range(2)]
-    h_raw = torch.empty(2 * n_max, dtype=torch.uint8).pin_memory()
     s0, s1 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     modes = {"exact": uz.UZIP_PIPE_EXACT, "sized": uz.UZIP_PIPE_SIZED, "streamed": uz.UZIP_PIPE_STREAMED,
              "bound": uz.UZIP_PIPE_BOUND, "serial": uz.UZIP_PIPE_SERIAL}
-    sizes = [1 << 15, 1 << 17, 1 << 19, 1 << 21, 1 << 23, 1 << 25, 1 << 27, n_max]  # values (64 KiB .. 1 GiB)
-    sweep = []
-    for n in sizes:
-        reps = int(max(4, min(64, (4 << 30) // (2 * n))))
-        if n == n_max:
-            reps = args.pipeline_messages
-        hs = torch.zeros(reps, dtype=torch.int64).pin_memory()
-        row = {"message_bytes": 2 * n, "messages": reps}
-        for name, mode in modes.items():
-            for it in range(2):  # first pass warms up
-                torch.cuda.synchronize(dev)
-                t0 = time.perf_counter()
-                st = uz.uzip_pipeline_send(uz.UZIP_BF16, [x.data_ptr()] * reps, [n] * reps,
-                                           [b.data_ptr() for b in banks], cap, [h.data_ptr() for h in hb], hcap,
-                                           hs.data_ptr(), mode, s0.cuda_stream, s1.cuda_stream)
-                torch.cuda.synchronize(dev)
-                dt = time.perf_counter() - t0
-                if st != 0:
-                    raise RuntimeError(f"pipeline status {st}")
-            row[name + "_gbs"] = reps * 2 * n / dt / 1e9
-        row["ratio"] = int(hs[0]) / (2 * n)
-        # plain copy of the raw bytes over the same link
-        raw = x.view(torch.uint8)[: 2 * n]
+
+    def send(ptrs, elems, mode, h_sizes, raw_below):
+        for it in range(2):  # the first pass warms up
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            st = uz.uzip_pipeline_send_ex(uz.UZIP_BF16, ptrs, elems, [b.data_ptr() for b in banks], cap,
+                                          [h.data_ptr() for h in hb], hcap, h_sizes.data_ptr(), mode, raw_below,
+                                          s0.cuda_stream, s1.cuda_stream)
+            torch.cuda.synchronize(dev)
+            dt = time.perf_counter() - t0
+            if st != 0:
+                raise RuntimeError(f"pipeline status {st}")
+        return dt
+
+    def raw_copy(views):
         for it in range(2):
             torch.cuda.synchronize(dev)
             t0 = time.perf_counter()
             with torch.cuda.stream(s1):
-                for _ in range(reps):
-                    h_raw[: 2 * n].copy_(raw, non_blocking=True)
+                for k, v in enumerate(views):
+                    hb[k & 1][: v.numel()].copy_(v, non_blocking=True)
             torch.cuda.synchronize(dev)
             dt = time.perf_counter() - t0
-        row["raw_d2h_gbs"] = reps * 2 * n / dt / 1e9
+        return dt
+
+    total_bytes = 2 * sum(sizes)
+    hs = torch.zeros(len(sizes), dtype=torch.int64).pin_memory()
+    stream_row = {"messages": len(sizes), "input_bytes": total_bytes}
+    for name, mode in modes.items():
+        dt = send([m.data_ptr() for m in msgs], sizes, mode, hs, uz.UZIP_PIPE_RAW_BELOW_DEFAULT)
+        stream_row[name + "_gbs"] = total_bytes / dt / 1e9
+    stream_row["compressed_bytes"] = int(hs.sum())
+    stream_row["ratio"] = int(hs.sum()) / total_bytes
+    stream_row["raw_d2h_gbs"] = total_bytes / raw_copy([m.view(torch.uint8) for m in msgs]) / 1e9
+    # message-size sweep on prefixes of message 0
+    x = msgs[0]
+    sweep = []
+    for n in [1 << 15, 1 << 17, 1 << 19, 1 << 21, 1 << 23, 1 << 24, 1 << 25, 1 << 27, n_max]:
+        reps = int(max(4, min(64, (4 << 30) // (2 * n))))
+        hsw = torch.zeros(reps, dtype=torch.int64).pin_memory()
+        row = {"message_bytes": 2 * n, "messages": reps,
+               "raw_container": 2 * n < uz.UZIP_PIPE_RAW_BELOW_DEFAULT}
+        for name in ("sized", "exact"):
+            row[name + "_gbs"] = reps * 2 * n / send([x.data_ptr()] * reps, [n] * reps, modes[name], hsw,
+                                                     uz.UZIP_PIPE_RAW_BELOW_DEFAULT) / 1e9
+        row["sized_coded_gbs"] = reps * 2 * n / send([x.data_ptr()] * reps, [n] * reps, modes["sized"], hsw, 0) / 1e9
+        row["raw_d2h_gbs"] = reps * 2 * n / raw_copy([x.view(torch.uint8)[: 2 * n]] * reps) / 1e9
         sweep.append(row)
     # one 1 GiB message, from the call to its last byte on the host
-    hs1 = torch.zeros(1, dtype=torch.int64).pin_memory()
     latency = {}
     for name in ("sized", "streamed"):
         best = float("inf")
@@ -370,22 +592,19 @@ def run_pipeline(args, dev):
             torch.cuda.synchronize(dev)
             t0 = time.perf_counter()
             st = uz.uzip_pipeline_send(uz.UZIP_BF16, [x.data_ptr()], [n_max], [b.data_ptr() for b in banks], cap,
-                                       [h.data_ptr() for h in hb], hcap, hs1.data_ptr(), modes[name], s0.cuda_stream,
+                                       [h.data_ptr() for h in hb], hcap, hs.data_ptr(), modes[name], s0.cuda_stream,
                                        s1.cuda_stream)
             torch.cuda.synchronize(dev)
             best = min(best, time.perf_counter() - t0)
             if st != 0:
                 raise RuntimeError(f"pipeline status {st}")
         latency[name + "_ms"] = best * 1e3
-    full = sweep[-1]
-    return {"one_message_latency": latency,
-            "workload": "c5: first 1 GiB message of the Llama-3-8B-shaped bf16 parameter set ~ N(0, 0.02), "
-                        f"sent {full['messages']} times; size sweep on its prefixes",
-            "unit": "GB/s (input bytes, host wall clock incl. sync)", "sweep": sweep,
-            "exact_gbs": full["exact_gbs"], "sized_gbs": full["sized_gbs"], "streamed_gbs": full["streamed_gbs"],
-            "bound_gbs": full["bound_gbs"],
-            "serial_gbs": full["serial_gbs"],
-            "raw_d2h_gbs": full["raw_d2h_gbs"]}
+    del banks
+    return {"workload": "c5: all 15 messages (8,030,261,248 bf16 values, 16.06 GB) of the Llama-3-8B-shaped "
+                        "parameter set ~ N(0, 0.02), one call per mode; size sweep on prefixes of message 0",
+            "unit": "GB/s (input bytes, host wall clock incl. sync)", "generation_s": t_gen,
+            "raw_below_bytes_default": uz.UZIP_PIPE_RAW_BELOW_DEFAULT, "stream": stream_row, "sweep": sweep,
+            "one_message_latency": latency}, msgs
 
 
 def run_gate(args, dev, x, n, peak):
@@ -512,23 +731,6 @@ def run_dtype_sweep(args, dev, peak):
     return {"workload": "one 256 MiB tensor per format ~ N(0, 0.02) (UCCL-Zip Fig. 12 format sweep)", "rows": rows}
 
 
-def cpu_baseline(bits):
-    """The oracle (single-threaded C) on a bounded sample of the tensor (the
-    first 2048 chunks), compress + decompress."""
-    import oracle
-
-    sample = bits[: 2048 * 65536]
-    t0 = time.perf_counter()
-    c = oracle.compress(sample)
-    t1 = time.perf_counter()
-    oracle.decompress(c, oracle.BF16, sample.size)
-    t2 = time.perf_counter()
-    return {"value": 2 * sample.size / (t2 - t0) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {sample.size} values of the workload ({sample.size // 65536} chunks), "
-                      f"compress {t1 - t0:.2f} s + decompress {t2 - t1:.2f} s",
-            "compress_gbs": 2 * sample.size / (t1 - t0) / 1e9, "decompress_gbs": 2 * sample.size / (t2 - t1) / 1e9}
-
-
 def run_reference(args):
     """Reference arm: the oracle on the host cores, each step one bounded sample
     (the first 256 chunks, 16,777,216 values) of the same workload."""
@@ -567,8 +769,7 @@ def main():
     ap.add_argument("--no-pipeline", action="store_true")
     ap.add_argument("--no-dtypes", action="store_true", help="skip the fp16/fp32/fp8 format sweep")
     ap.add_argument("--no-gate", action="store_true", help="skip the whole-message RAW / gate measurement")
-    ap.add_argument("--pipeline-messages", type=int, default=8,
-                    help="1 GiB messages sent through the split-send pipeline")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config table (c1, c2, c3, c5)")
     ap.add_argument("--elements", type=int, default=None,
                     help="use only the first N values of the workload (profiling captures)")
     args = ap.parse_args()

@@ -17,14 +17,18 @@
  *                   16 zero bytes
  *   [64, 64+8C)     u64 offset of chunk c's stream, relative to exp_offset
  *   [64+8C, 64+12C) u32 length of chunk c's stream, bit 31 = stored RAW
- *   rem_offset = round16(64 + 12C): remainder plane in element order, the
- *                   sign placed just above the fraction: bf16 1 byte
- *                   (sign<<7 | fraction), fp16 2 bytes (sign<<10 |
- *                   fraction), fp32 3 bytes (sign<<23 | fraction), fp8
- *                   e4m3fn / e5m2 one 4-bit field (sign<<3 | fraction,
- *                   sign<<2 | fraction) per element, two per byte, element
- *                   2j in the low nibble of byte j; multi-byte fields are
- *                   little endian.  P = its size in bytes.
+ *   rem_offset = round16(64 + 12C): the remainder plane.  Each element
+ *                   contributes a w-bit field, its sign placed just above
+ *                   its fraction: bf16 w = 8 (sign<<7 | fraction),
+ *                   fp32 w = 24 (sign<<23 | fraction), fp16 w = 11
+ *                   (sign<<10 | fraction), fp8 e4m3fn w = 4 (sign<<3 |
+ *                   fraction), fp8 e5m2 w = 3 (sign<<2 | fraction).  The
+ *                   fields are packed back to back, least significant bit
+ *                   first: element i occupies bits [w*i, w*i + w) of the
+ *                   plane, where bit k of the plane is bit k % 8 of byte
+ *                   k / 8; bits past the last field are zero.  For bf16 this
+ *                   is one byte per element and for fp32 three little-endian
+ *                   bytes.  P = ceil(n * w / 8) bytes.
  *   exp_offset = round16(rem_offset + P): one stream per chunk, each
  *                   starting 16-byte aligned and zero padded to 16 bytes.
  *   The exponent field (8 bits for bf16 and fp32, 5 for fp16 and e5m2, 4
@@ -71,7 +75,7 @@ typedef enum {
 typedef enum {
     UZIP_OK = 0,
     UZIP_ERR_INVALID_ARG = 1,       /* null or misaligned pointer, n too large */
-    UZIP_ERR_UNSUPPORTED_DTYPE = 2, /* dtype not bf16 / fp32 */
+    UZIP_ERR_UNSUPPORTED_DTYPE = 2, /* dtype is not one of the five uzip_dtype values */
     UZIP_ERR_CAPACITY = 3,          /* output buffer smaller than required */
     UZIP_ERR_CORRUPT = 4,           /* container failed validation */
     UZIP_ERR_TIMEOUT = 5,           /* a bounded device-side wait ran out */
@@ -82,7 +86,11 @@ typedef enum {
 /* Largest number of elements one call accepts (2^40). */
 #define UZIP_MAX_ELEMS (1ull << 40)
 
-/* Bytes the output buffer of uzip_compress must hold for (dtype, n): the
+/* Bytes the output buffer of uzip_compress must hold for (dtype, n).  The
+ * container itself is a self-describing frame whose header states its size
+ * (NCCLZ, arXiv 2605.12396, Sec. IV-B and IV-D2: a frame header carrying the
+ * payload byte count ahead of the payload); the buffer also holds the
+ * compressor's work area behind the largest frame.  In detail: the
  * largest possible container (every chunk stored RAW, rounded up to 16) plus
  * the compressor's work area behind it: 16 + 8*C bytes of counters and chunk
  * descriptors, 256 bytes of alignment slack and min(C, 1536) pairs of 68 KiB
@@ -92,7 +100,8 @@ typedef enum {
 uint64_t uzip_max_compressed_size(uzip_dtype dtype, uint64_t n);
 
 /* Compress n elements at d_in into the container at d_out.
- *   d_in          device, 16-byte aligned, n * (2 or 4) bytes; may be NULL
+ *   d_in          device, 16-byte aligned, n * element bytes (2 for bf16
+ *                 and fp16, 4 for fp32, 1 for fp8); may be NULL
  *                 when n == 0.
  *   d_out         device, 16-byte aligned, out_capacity bytes; must be at
  *                 least uzip_max_compressed_size(dtype, n) (else
@@ -165,7 +174,7 @@ uzip_status uzip_compress_noalloc(const void* d_in, uzip_dtype dtype, uint64_t n
 /* Decompress the container at d_comp into n elements at d_out.
  *   d_comp         device, 16-byte aligned; comp_capacity = readable bytes
  *                  (at least the container's total_bytes).
- *   d_out          device, 16-byte aligned, n * (2 or 4) bytes.
+ *   d_out          device, 16-byte aligned, n * element bytes (1, 2 or 4).
  *   d_status       device i32 (nullable): set to 0, then to UZIP_ERR_CORRUPT
  *                  if any check fails: header fields against (dtype, n),
  *                  chunk offsets and lengths in range, frequency table sums
@@ -195,7 +204,9 @@ uzip_status uzip_compress_gated(const void* d_in, uzip_dtype dtype, uint64_t n, 
                                 uint64_t raw_below_bytes, cudaStream_t s);
 
 /* Read the 64-byte header of the container at d_comp (device) and return
- * its total size, dtype and element count.  Synchronises s.  Returns
+ * its total size, dtype and element count (NCCLZ Sec. IV-B and IV-D2: the
+ * receiver learns the payload size and codec from the frame header before it
+ * touches the payload).  Synchronises s.  Returns
  * UZIP_ERR_CORRUPT if the magic, version or layout fields do not check out,
  * or total_bytes == 0 (a failed compression). Any output pointer may be NULL. */
 uzip_status uzip_query_size(const void* d_comp, uint64_t* h_total_bytes, uzip_dtype* h_dtype,
@@ -217,6 +228,10 @@ const char* uzip_status_string(uzip_status st);
  *                            h_capacity bytes each; message k's container
  *                            lands in h_bank[k % 2] (a later message reuses
  *                            the bank, as a sender's staging buffer would).
+ *                            A message of fewer than
+ *                            UZIP_PIPE_RAW_BELOW_DEFAULT input bytes travels
+ *                            as a whole-message RAW container (see
+ *                            uzip_pipeline_send_ex).
  *   h_sizes                  pinned host u64[n_msgs]: container size of each
  *                            message, written by the device (0 on failure).
  *   mode                     UZIP_PIPE_EXACT: a copy kernel reads the size on
@@ -260,6 +275,28 @@ uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d_msgs, cons
                                uint32_t n_msgs, void* const* d_bank, uint64_t bank_capacity,
                                void* const* h_bank, uint64_t h_capacity, uint64_t* h_sizes,
                                uzip_pipe_mode mode, cudaStream_t s_compress, cudaStream_t s_copy);
+
+/* uzip_pipeline_send sends a message smaller than this many input bytes as a
+ * whole-message RAW container (every chunk stored RAW, no statistics or
+ * coding; NCCLZ Sec. IV-C: a message whose coding would not pay travels RAW):
+ * below it, coding one message takes longer than copying its raw bytes. */
+#define UZIP_PIPE_RAW_BELOW_DEFAULT (32ull << 20)
+
+/* The split-send pipeline with every choice explicit:
+ *   h_bank[n_hbanks]  n_hbanks >= 2 pinned host banks; message k's container
+ *                     lands in h_bank[k % n_hbanks] (with n_hbanks = n_msgs
+ *                     every container stays on the host); the device banks
+ *                     stay two.
+ *   raw_below_bytes   a message of fewer input bytes travels as a
+ *                     whole-message RAW container (its streamed mode falls
+ *                     back to the sized copy); 0 codes every message.
+ * Everything else is as for uzip_pipeline_send, which is this call with
+ * n_hbanks = 2 and raw_below_bytes = UZIP_PIPE_RAW_BELOW_DEFAULT. */
+uzip_status uzip_pipeline_send_ex(uzip_dtype dtype, const void* const* d_msgs, const uint64_t* msg_elems,
+                                  uint32_t n_msgs, void* const* d_bank, uint64_t bank_capacity,
+                                  void* const* h_bank, uint32_t n_hbanks, uint64_t h_capacity,
+                                  uint64_t* h_sizes, uzip_pipe_mode mode, uint64_t raw_below_bytes,
+                                  cudaStream_t s_compress, cudaStream_t s_copy);
 
 #ifdef __cplusplus
 }

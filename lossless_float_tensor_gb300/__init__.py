@@ -1,4 +1,5 @@
-"""Python binding of libuzip: lossless compression of bf16 / fp32 GPU tensors.
+"""Python binding of libuzip: lossless compression of bf16, fp16, fp32 and fp8
+GPU tensors.
 
 Thin ctypes layer over the C ABI in include/uzip.h.  The functions named like
 the C entry points (uzip_compress, ...) only marshal arguments: every step of
@@ -28,6 +29,7 @@ UZIP_NOALLOC_MAX_ELEMS = 1 << 30
 UZIP_TESTFLAG_SKIP_CHUNK0 = 1
 UZIP_FLAG_SAMPLED_TABLES = 2
 UZIP_PIPE_EXACT, UZIP_PIPE_BOUND, UZIP_PIPE_SERIAL, UZIP_PIPE_SIZED, UZIP_PIPE_STREAMED = 0, 1, 2, 3, 4
+UZIP_PIPE_RAW_BELOW_DEFAULT = 32 << 20
 UZIP_MAX_ELEMS = 1 << 40
 CHUNK_ELEMS = 65536
 HEADER_BYTES = 64
@@ -57,6 +59,9 @@ _lib.uzip_status_string.restype = ctypes.c_char_p
 _lib.uzip_pipeline_send.argtypes = [_int, ctypes.POINTER(_vp), ctypes.POINTER(_u64), _u32, ctypes.POINTER(_vp), _u64,
                                     ctypes.POINTER(_vp), _u64, _vp, _int, _vp, _vp]
 _lib.uzip_pipeline_send.restype = _int
+_lib.uzip_pipeline_send_ex.argtypes = [_int, ctypes.POINTER(_vp), ctypes.POINTER(_u64), _u32, ctypes.POINTER(_vp), _u64,
+                                       ctypes.POINTER(_vp), _u32, _u64, _vp, _int, _u64, _vp, _vp]
+_lib.uzip_pipeline_send_ex.restype = _int
 _lib.uzip_debug_div_magic.argtypes = [_u32, ctypes.POINTER(_u32), ctypes.POINTER(_u32), ctypes.POINTER(_u32)]
 _lib.uzip_debug_div_magic.restype = _int
 _lib.uzip_debug_scratch_offset.argtypes = [_int, _u64]
@@ -123,6 +128,18 @@ def uzip_pipeline_send(dtype: int, d_msgs, msg_elems, d_bank, bank_capacity: int
     hb = (_vp * 2)(*h_bank)
     return int(_lib.uzip_pipeline_send(dtype, msgs, elems, k, db, bank_capacity, hb, h_capacity, h_sizes, mode,
                                        s_compress, s_copy))
+
+
+def uzip_pipeline_send_ex(dtype: int, d_msgs, msg_elems, d_bank, bank_capacity: int, h_bank, h_capacity: int,
+                          h_sizes: int, mode: int, raw_below_bytes: int, s_compress: int, s_copy: int) -> int:
+    k = len(d_msgs)
+    msgs = (_vp * k)(*d_msgs)
+    elems = (_u64 * k)(*msg_elems)
+    db = (_vp * 2)(*d_bank)
+    nh = len(h_bank)
+    hb = (_vp * nh)(*h_bank)
+    return int(_lib.uzip_pipeline_send_ex(dtype, msgs, elems, k, db, bank_capacity, hb, nh, h_capacity, h_sizes, mode,
+                                          raw_below_bytes, s_compress, s_copy))
 
 
 # ---- torch convenience layer (allocation and streams only) ----------------

@@ -244,6 +244,16 @@ int uzip_debug_div_magic(uint32_t f, uint32_t* m, uint32_t* add, uint32_t* shift
     return int(d.ok);
 }
 
+int uzip_debug_div_magic33(uint32_t f, uint32_t* m_lo, uint32_t* shift) {
+    if (f == 0 || f > kM) return 0;
+    const Magic33 d = magic33(f);
+    if (m_lo) *m_lo = d.m_lo;
+    if (shift) *shift = d.sh;
+    return 1;
+}
+
+void uzip_debug_set_ws_jit_blocks(uint32_t blocks) { g_ws_jit_blocks = blocks; }
+
 uint64_t uzip_debug_scratch_offset(uzip_dtype dtype, uint64_t n) {
     if (!valid_dtype(dtype) || n > UZIP_MAX_ELEMS) return 0;
     return scratch_offset(dtype, n);

@@ -7,6 +7,9 @@
 
 namespace uzip {
 
+// tuning of the warp-specialised compressor (see CompressArgs::jit_blocks)
+uint32_t g_ws_jit_blocks = 32;
+
 extern template cudaError_t launch_mode<UZIP_BF16>(CompressArgs, int, bool, cudaStream_t);
 extern template cudaError_t launch_mode<UZIP_FP32>(CompressArgs, int, bool, cudaStream_t);
 extern template cudaError_t launch_mode<UZIP_FP16>(CompressArgs, int, bool, cudaStream_t);
@@ -40,6 +43,7 @@ cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n
     a.stash = static_cast<uint8_t*>(stash);
     a.gated = 0;
     a.progress = progress;
+    a.jit_blocks = g_ws_jit_blocks;
     const bool has_stash = stash != nullptr;
     switch (dtype) {
         case UZIP_BF16: return launch_mode<UZIP_BF16>(a, mode, has_stash, s);
@@ -55,7 +59,7 @@ cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n
 cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                             int32_t* d_status, uint32_t first_ticket, cudaStream_t s, int mode, uint64_t* progress) {
     uint8_t* work = static_cast<uint8_t*>(d_out) + scratch_offset(dtype, n);
-    const uintptr_t st = (reinterpret_cast<uintptr_t>(work) + scratch_bytes(n) + 255) & ~uintptr_t(255);
+    const uintptr_t st = (reinterpret_cast<uintptr_t>(work) + scratch_bytes(n) + 4095) & ~uintptr_t(4095);
     return launch_compress_with_scratch(dtype, d_in, n, d_out, d_out_size, d_status, first_ticket, work,
                                         reinterpret_cast<void*>(st), s, mode, progress);
 }

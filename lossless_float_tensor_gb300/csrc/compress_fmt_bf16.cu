@@ -1,5 +1,5 @@
 // Compressor kernels for one element format (bf16).
-#include "compress_kernels.cuh"
+#include "compress_ws.cuh"
 
 namespace uzip {
 template cudaError_t launch_mode<UZIP_BF16>(CompressArgs, int, bool, cudaStream_t);

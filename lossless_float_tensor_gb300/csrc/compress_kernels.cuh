@@ -43,6 +43,10 @@ struct CompressArgs {
     // remainder plane is written and progress[2c + 1] = 2^63 | (end of its
     // stream in the exponent section) once the stream is in place
     uint64_t* progress;
+    // warp-specialised compressor: a helper starts splitting its next chunk
+    // once its encoder has at most this many blocks of 32 steps left of the
+    // current one (64 or more: at once)
+    uint32_t jit_blocks;
 };
 
 // element traits --------------------------------------------------------------
@@ -749,16 +753,16 @@ inline __device__ void write_stream_head(uint8_t* dst, uint32_t x, const Norm& n
         if (nm.present & (1u << k)) d16[80 + idx++] = uint16_t(nm.f[k]);
 }
 
-// Copies the record [start, kSlotBytes) of a slot (start 2-byte aligned) to dst
-// (16-byte aligned) in 16-byte blocks, zero padding the last block; 4
-// blocks in flight per lane.
+// Copies the record [start, end) of a slot (start 2-byte aligned, end 4-byte
+// aligned) to dst (16-byte aligned) in 16-byte blocks, zero padding the last
+// block; 4 blocks in flight per lane.
 inline __device__ void copy_record_from_slot(const uint8_t* slot, uint32_t start, uint8_t* dst, uint32_t lane,
-                                      uint64_t pol) {
-    const uint32_t len = kSlotBytes - start;
+                                      uint64_t pol, uint32_t end = kSlotBytes) {
+    const uint32_t len = end - start;
     const uint32_t nb = (len + 15) / 16;
     const uint32_t mis = start & 2u;  // start mod 4 is 0 or 2
     const uint32_t* wbase = reinterpret_cast<const uint32_t*>(slot + (start & ~3u));
-    const uint32_t nwords = (kSlotBytes - (start & ~3u)) / 4;  // words of the slot from wbase on
+    const uint32_t nwords = (end - (start & ~3u)) / 4;  // words of the slot from wbase on
     for (uint32_t b0 = 0; b0 < nb; b0 += 4 * 32) {
         uint32_t w[4][5];
 #pragma unroll
@@ -1231,8 +1235,15 @@ __global__ void __launch_bounds__(32) raw_kernel(CompressArgs a) {
 // ---------------------------------------------------------------------------
 // launcher of one format and mode (instantiated in compress_fmt_*.cu)
 
+// the warp-specialised compressor (compress_ws.cuh)
+template <int DT>
+cudaError_t launch_ws(const CompressArgs& a, cudaStream_t s);
+
 // Launches the kernels of one compression mode (0: per-chunk choice, 1: whole
-// message RAW, 2: gated) for element format DT.
+// message RAW, 2: gated, 3: sampled tables) for element format DT.  With a
+// slot area, modes 0 and 2 code with the warp-specialised compressor; the
+// sampled tables, and every mode without a slot area (the allocation-free
+// entry point), use the one-warp compressor.
 template <int DT>
 cudaError_t launch_mode(CompressArgs a, int mode, bool stash, cudaStream_t s) {
     cudaError_t err;
@@ -1253,6 +1264,7 @@ cudaError_t launch_mode(CompressArgs a, int mode, bool stash, cudaStream_t s) {
         raw_kernel<DT><<<dim3(uint32_t(grid)), dim3(32), 0, s>>>(a);
         if ((err = cudaGetLastError()) != cudaSuccess || mode == 1) return err;
     }
+    if ((mode == 0 || mode == 2) && stash && C > 0) return launch_ws<DT>(a, s);
     void (*kern)(CompressArgs) = mode == 3 ? compress_kernel<DT, true> : compress_kernel<DT, false>;
     if ((err = launch_shape(reinterpret_cast<const void*>(kern), 32, kCompressSmem, &sms, &per_sm)) != cudaSuccess)
         return err;

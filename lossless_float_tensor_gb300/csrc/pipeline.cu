@@ -96,13 +96,15 @@ cudaError_t stream_out(int dtype, uint64_t n, const uint8_t* db, uint8_t* hb, ui
 }
 }  // namespace
 
-extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d_msgs, const uint64_t* msg_elems,
-                                          uint32_t n_msgs, void* const* d_bank, uint64_t bank_capacity,
-                                          void* const* h_bank, uint64_t h_capacity, uint64_t* h_sizes,
-                                          uzip_pipe_mode mode, cudaStream_t s_compress, cudaStream_t s_copy) {
+extern "C" uzip_status uzip_pipeline_send_ex(uzip_dtype dtype, const void* const* d_msgs, const uint64_t* msg_elems,
+                                             uint32_t n_msgs, void* const* d_bank, uint64_t bank_capacity,
+                                             void* const* h_bank, uint32_t n_hbanks, uint64_t h_capacity,
+                                             uint64_t* h_sizes, uzip_pipe_mode mode, uint64_t raw_below_bytes,
+                                             cudaStream_t s_compress, cudaStream_t s_copy) {
     using namespace uzip;
     if (!valid_dtype(dtype)) return UZIP_ERR_UNSUPPORTED_DTYPE;
-    if (n_msgs == 0 || !d_msgs || !msg_elems || !d_bank || !h_bank || !h_sizes) return UZIP_ERR_INVALID_ARG;
+    if (n_msgs == 0 || !d_msgs || !msg_elems || !d_bank || !h_bank || !h_sizes || n_hbanks < 2)
+        return UZIP_ERR_INVALID_ARG;
     if (mode != UZIP_PIPE_EXACT && mode != UZIP_PIPE_BOUND && mode != UZIP_PIPE_SERIAL && mode != UZIP_PIPE_SIZED &&
         mode != UZIP_PIPE_STREAMED)
         return UZIP_ERR_INVALID_ARG;
@@ -116,14 +118,16 @@ extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d
     // streamed: the host banks also hold 16 bytes of progress per chunk
     const uint64_t prog_off = round16(container_bound(dtype, largest));
     if (mode == UZIP_PIPE_STREAMED && h_capacity < prog_off + 16 * num_chunks(largest)) return UZIP_ERR_CAPACITY;
-    void* h_dev[2] = {nullptr, nullptr};
     void* sizes_dev = nullptr;
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 2; ++b)
         if (!d_bank[b] || (reinterpret_cast<uintptr_t>(d_bank[b]) & 15)) return UZIP_ERR_INVALID_ARG;
-        if (!host_mapped(h_bank[b], &h_dev[b]) || (reinterpret_cast<uintptr_t>(h_dev[b]) & 15))
-            return UZIP_ERR_INVALID_ARG;
+    for (uint32_t b = 0; b < n_hbanks; ++b) {
+        void* hd = nullptr;
+        if (!host_mapped(h_bank[b], &hd) || (reinterpret_cast<uintptr_t>(hd) & 15)) return UZIP_ERR_INVALID_ARG;
+        for (uint32_t b2 = 0; b2 < b; ++b2)
+            if (h_bank[b2] == h_bank[b]) return UZIP_ERR_INVALID_ARG;
     }
-    if (d_bank[0] == d_bank[1] || h_bank[0] == h_bank[1]) return UZIP_ERR_INVALID_ARG;
+    if (d_bank[0] == d_bank[1]) return UZIP_ERR_INVALID_ARG;
     if (!host_mapped(h_sizes, &sizes_dev) || (reinterpret_cast<uintptr_t>(sizes_dev) & 7)) return UZIP_ERR_INVALID_ARG;
 
     const bool serial = mode == UZIP_PIPE_SERIAL;
@@ -137,21 +141,39 @@ extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d
             result = UZIP_ERR_CUDA;
     }
     for (uint32_t k = 0; k < n_msgs && result == UZIP_OK; ++k) {
-        const int b = int(k & 1u);
+        const int b = int(k & 1u);          // device bank
+        void* hb = h_bank[k % n_hbanks];    // host bank
+        void* hd = nullptr;                 // its device-side address
+        host_mapped(hb, &hd);
+        // whole-message RAW below the threshold (NCCLZ Sec. IV-C: a message
+        // whose coding does not pay travels RAW); such a message is copied
+        // with the sized scheme when the streamed one is asked for
+        const bool raw_msg = msg_elems[k] * elem_bytes(dtype) < raw_below_bytes;
+        const uzip_pipe_mode mk = (raw_msg && mode == UZIP_PIPE_STREAMED) ? UZIP_PIPE_SIZED : mode;
         // bank b still holds message k-2 until its copy has finished
         if (k >= 2 && !serial && cudaStreamWaitEvent(sc, copied[b], 0) != cudaSuccess) {
             result = UZIP_ERR_CUDA;
             break;
         }
-        if (mode == UZIP_PIPE_STREAMED) {
+        if (raw_msg) {
+            if (msg_elems[k] > 0 && (!d_msgs[k] || (reinterpret_cast<uintptr_t>(d_msgs[k]) & 15))) {
+                result = UZIP_ERR_INVALID_ARG;
+                break;
+            }
+            if (launch_compress(dtype, d_msgs[k], msg_elems[k], d_bank[b], static_cast<uint64_t*>(sizes_dev) + k, nullptr,
+                                0, sc, 1) != cudaSuccess) {
+                result = UZIP_ERR_CUDA;
+                break;
+            }
+        } else if (mk == UZIP_PIPE_STREAMED) {
             // progress words live past the container in the host bank
-            volatile uint64_t* prog = reinterpret_cast<volatile uint64_t*>(static_cast<uint8_t*>(h_bank[b]) + prog_off);
+            volatile uint64_t* prog = reinterpret_cast<volatile uint64_t*>(static_cast<uint8_t*>(hb) + prog_off);
             for (uint64_t i = 0; i < 2 * num_chunks(msg_elems[k]); ++i) prog[i] = 0;
             if (msg_elems[k] > 0 && (!d_msgs[k] || (reinterpret_cast<uintptr_t>(d_msgs[k]) & 15))) {
                 result = UZIP_ERR_INVALID_ARG;
                 break;
             }
-            uint64_t* prog_dev = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(h_dev[b]) + prog_off);
+            uint64_t* prog_dev = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(hd) + prog_off);
             if (launch_compress(dtype, d_msgs[k], msg_elems[k], d_bank[b], static_cast<uint64_t*>(sizes_dev) + k, nullptr,
                                 0, sc, 0, prog_dev) != cudaSuccess) {
                 result = UZIP_ERR_CUDA;
@@ -164,25 +186,25 @@ extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d
         }
         // streamed copies run while the kernel does: only they skip the wait
         if (!serial && (cudaEventRecord(compressed[b], sc) != cudaSuccess ||
-                        (mode != UZIP_PIPE_STREAMED && cudaStreamWaitEvent(sx, compressed[b], 0) != cudaSuccess))) {
+                        (mk != UZIP_PIPE_STREAMED && cudaStreamWaitEvent(sx, compressed[b], 0) != cudaSuccess))) {
             result = UZIP_ERR_CUDA;
             break;
         }
         cudaError_t err = cudaSuccess;
-        if (mode == UZIP_PIPE_STREAMED) {
-            err = stream_out(dtype, msg_elems[k], static_cast<const uint8_t*>(d_bank[b]),
-                             static_cast<uint8_t*>(h_bank[b]), prog_off, compressed[b], sx);
-        } else if (mode == UZIP_PIPE_BOUND) {
-            err = cudaMemcpyAsync(h_bank[b], d_bank[b], container_bound(dtype, msg_elems[k]), cudaMemcpyDeviceToHost, sx);
-        } else if (mode == UZIP_PIPE_SIZED) {
+        if (mk == UZIP_PIPE_STREAMED) {
+            err = stream_out(dtype, msg_elems[k], static_cast<const uint8_t*>(d_bank[b]), static_cast<uint8_t*>(hb),
+                             prog_off, compressed[b], sx);
+        } else if (mk == UZIP_PIPE_BOUND) {
+            err = cudaMemcpyAsync(hb, d_bank[b], container_bound(dtype, msg_elems[k]), cudaMemcpyDeviceToHost, sx);
+        } else if (mk == UZIP_PIPE_SIZED) {
             // the size is known once this compression is done; message k-1's
             // copy keeps running on s_copy meanwhile
             err = cudaEventSynchronize(compressed[b]);
             const uint64_t total = *reinterpret_cast<volatile const uint64_t*>(h_sizes + k);
             if (err == cudaSuccess && total > 0)
-                err = cudaMemcpyAsync(h_bank[b], d_bank[b], total, cudaMemcpyDeviceToHost, sx);
+                err = cudaMemcpyAsync(hb, d_bank[b], total, cudaMemcpyDeviceToHost, sx);
         } else {
-            err = launch_copy_exact(d_bank[b], h_dev[b], sx);
+            err = launch_copy_exact(d_bank[b], hd, sx);
         }
         if (err == cudaSuccess && !serial) err = cudaEventRecord(copied[b], sx);
         if (err != cudaSuccess) result = UZIP_ERR_CUDA;
@@ -193,4 +215,12 @@ extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d
     }
     if (result == UZIP_ERR_CUDA) cudaGetLastError();
     return result;
+}
+
+extern "C" uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d_msgs, const uint64_t* msg_elems,
+                                          uint32_t n_msgs, void* const* d_bank, uint64_t bank_capacity,
+                                          void* const* h_bank, uint64_t h_capacity, uint64_t* h_sizes,
+                                          uzip_pipe_mode mode, cudaStream_t s_compress, cudaStream_t s_copy) {
+    return uzip_pipeline_send_ex(dtype, d_msgs, msg_elems, n_msgs, d_bank, bank_capacity, h_bank, 2, h_capacity,
+                                 h_sizes, mode, UZIP_PIPE_RAW_BELOW_DEFAULT, s_compress, s_copy);
 }

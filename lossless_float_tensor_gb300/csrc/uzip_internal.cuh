@@ -88,24 +88,26 @@ constexpr uint64_t kScratchHead = 16;
 __host__ __device__ inline uint64_t scratch_offset(int dtype, uint64_t n) { return round16(container_bound(dtype, n)); }
 // status, ticket, done counter and look-back descriptors (zeroed before each launch)
 __host__ __device__ inline uint64_t scratch_bytes(uint64_t n) { return kScratchHead + 8 * num_chunks(n); }
-// Slots: two slots of kSlotBytes per resident warp (at most kStashWarps
-// warps), used in turn.  A full chunk's exponent bytes fill the first 64 KiB
-// of a slot; its rANS words grow downwards from the slot's end, so the 4 KiB
-// beyond the exponent bytes keep the first words clear of bytes not yet read.
-// The finished stream then waits at the slot's end for its offset while the
-// warp counts its next chunk in the other slot.  Slots are never read before
-// they are written.
-constexpr uint64_t kStashWarps = 1536;
+// Slot area, at the first 4 KiB-aligned address (absolute) after the
+// descriptors (4 KiB of slack cover the alignment), in slots of kSlotBytes: a
+// chunk's exponent bytes fill the first 64 KiB of a slot and its rANS words
+// grow down from the slot's end over exponent bytes already read (the 4 KiB
+// beyond the exponent bytes keep the first words clear of bytes not yet
+// read); the finished record waits there for its offset.  The
+// warp-specialised compressor gives each of its kWsEnc encoders per block two
+// slots (contexts), used in turn; the one-warp compressor (sampled tables)
+// gives each warp two.  Slots are never read before they are written.
+constexpr uint32_t kWsEnc = 8;                   // encoder warps per block of the warp-specialised compressor
+constexpr uint64_t kWsMaxCtas = 160;             // blocks the slot area is sized for
 constexpr uint32_t kSlotBytes = 65536 + 4096;
-__host__ __device__ inline uint64_t stash_warps(uint64_t n) {
-    const uint64_t c = num_chunks(n);
-    return c < kStashWarps ? c : kStashWarps;
+__host__ __device__ inline uint64_t ws_ctas(uint64_t n) {
+    const uint64_t c = (num_chunks(n) + kWsEnc - 1) / kWsEnc;
+    return c < kWsMaxCtas ? c : kWsMaxCtas;
 }
-// The slots start at the first 256-byte aligned address (absolute) after the
-// descriptors; 256 bytes of slack cover the alignment.
-__host__ __device__ inline uint64_t work_area_bytes(uint64_t n) {
-    return scratch_bytes(n) + 256 + stash_warps(n) * 2 * uint64_t(kSlotBytes);
-}
+__host__ __device__ inline uint64_t slot_area_bytes(uint64_t n) { return ws_ctas(n) * kWsEnc * 2 * uint64_t(kSlotBytes); }
+// one-warp compressor: warps whose two slots fit the area
+__host__ __device__ inline uint64_t stash_warps(uint64_t n) { return slot_area_bytes(n) / (2 * uint64_t(kSlotBytes)); }
+__host__ __device__ inline uint64_t work_area_bytes(uint64_t n) { return scratch_bytes(n) + 4096 + slot_area_bytes(n); }
 
 // look-back descriptor: flag in bits 62..63, byte count in bits 0..61
 constexpr uint64_t kDescAggregate = 1ull << 62;
@@ -180,6 +182,54 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
+// ---- asynchronous copies and barriers (inline PTX) --------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// bulk copy global -> shared, completing `bytes` of transaction on `bar`
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+// bulk copy shared -> global, tracked by bulk groups
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void l2_discard_line(const void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // Exact floor(x / f) for x in [16 f, f * 2^20) as (x * m + add) >> (32 + sh)
 // (Robison, "N-bit unsigned division via N-bit multiply-add", ARITH 2005).
 // With p = max(32, 31 + ceil(log2 f)) the reciprocal fits 32 bits; either the
@@ -238,6 +288,39 @@ constexpr MagicTable make_magic_table() {
     return t;
 }
 
+// Exact floor(x / f) for x in [0, f * 2^20) with a 33-bit reciprocal:
+// sh = ceil(log2 f) and m = ceil(2^(32 + sh) / f), which lies in [2^32, 2^33),
+// so m = 2^32 + m_lo and x m = x m_lo + x 2^32 is one 32 x 32 -> 64-bit
+// multiply-add.  With e = m f - 2^(32 + sh) < f, the error term x e / (f 2^(32
+// + sh)) stays below 1/f as long as x e < 2^(32 + sh); x < f 2^20 and
+// e < f <= 2^sh give x e < 2^(2 sh + 20) <= 2^(32 + sh) for sh <= 12, so
+// floor(x m / 2^(32 + sh)) = floor(x / f) for every f in [1, 4096] (Granlund
+// and Montgomery, "Division by invariant integers using multiplication",
+// PLDI 1994, with the extra multiplier bit folded into the addend).  The
+// product also stays below 2^64: x m < 2^(52 + sh) + f 2^20 <= 2^64.
+struct Magic33 {
+    uint32_t m_lo, sh;
+};
+__host__ __device__ constexpr inline Magic33 magic33(uint32_t f) {
+    Magic33 r{0u, 0u};
+    if (f == 0 || f > kM) return r;
+    uint32_t sh = 0;
+    while ((1u << sh) < f) ++sh;
+    const uint64_t two = 1ull << (32 + sh);
+    const uint64_t m = (two + f - 1) / f;
+    r.m_lo = uint32_t(m - (1ull << 32));
+    r.sh = sh;
+    return r;
+}
+struct Magic33Table {
+    Magic33 e[kM + 1];
+};
+constexpr Magic33Table make_magic33_table() {
+    Magic33Table t{};
+    for (uint32_t f = 1; f <= kM; ++f) t.e[f] = magic33(f);
+    return t;
+}
+
 // SM count and resident blocks per SM of `kern` on the current device, looked
 // up once per (device, kernel, block shape) and cached (api.cu).
 cudaError_t launch_shape(const void* kern, int threads, size_t smem, int* sms, int* per_sm);
@@ -253,6 +336,10 @@ cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out
 cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                                          int32_t* d_status, uint32_t first_ticket, void* scratch_area, void* stash,
                                          cudaStream_t s, int mode = 0, uint64_t* progress = nullptr);
+
+// warp-specialised compressor: blocks of its encoder's current chunk left when
+// a helper starts splitting the next one (compress.cu; a test hook sets it)
+extern uint32_t g_ws_jit_blocks;
 
 // allocation-free compression: largest tensor and device count served by the
 // library's own work area

@@ -48,7 +48,9 @@ def test_max_compressed_size_is_container_bound_plus_work_area(uz):
             bound = oracle.container_bound(dtype, n)
             off = uz.library().uzip_debug_scratch_offset(dtype, n)
             assert off == -(-bound // 16) * 16
-            work = 16 + 8 * c + 256 + min(c, 1536) * 2 * (65536 + 4096)  # counters, descriptors, two slots per warp
+            # counters and descriptors, 4 KiB of alignment slack, and two
+            # 68 KiB slots for each of the 8 encoders of up to 160 blocks
+            work = 16 + 8 * c + 4096 + min(-(-c // 8), 160) * 8 * 2 * 69632
             assert uz.uzip_max_compressed_size(dtype, n) == off + work
     assert uz.uzip_max_compressed_size(7, 10) == 0
     assert uz.uzip_max_compressed_size(0, (1 << 40) + 1) == 0
@@ -79,6 +81,31 @@ def test_division_magic_exact_for_every_frequency(uz):
             assert (((1 << 20) - 1) * f + 1) * (two_p - M * f) <= two_p
     assert lib.uzip_debug_div_magic(0, None, None, None) == 0
     assert lib.uzip_debug_div_magic(4097, None, None, None) == 0
+
+
+def test_33_bit_division_magic_exact_for_every_frequency(uz):
+    """The warp-specialised encoder divides by f as
+    (x * (2^32 + m_lo)) >> (32 + sh) for x in [0, f * 2^20): checked at the
+    worst points (x = k f - 1 at the top and bottom of the range), random x,
+    and against the closed-form error bound x e < 2^(32 + sh)."""
+    import ctypes
+
+    lib = uz.library()
+    m, sh = ctypes.c_uint32(), ctypes.c_uint32()
+    rng = random.Random(11)
+    for f in range(1, 4097):
+        assert lib.uzip_debug_div_magic33(f, ctypes.byref(m), ctypes.byref(sh)) == 1
+        M, S = (1 << 32) + m.value, sh.value
+        assert (1 << S) >= f and S <= 12 and (1 << 32) <= M < (1 << 33)
+        top = f << 20
+        xs = {0, 1, f - 1, f, top - 1, top - f, top - f - 1, top - 2 * f, top - 2 * f + 1, (1 << 16)}
+        xs |= {rng.randrange(0, top) for _ in range(24)}
+        for x in xs:
+            assert (x * M) >> (32 + S) == x // f, (f, x)
+            assert x * M < 1 << 64
+        assert (top - 1) * (M * f - (1 << (32 + S))) < 1 << (32 + S)
+    assert lib.uzip_debug_div_magic33(0, None, None) == 0
+    assert lib.uzip_debug_div_magic33(4097, None, None) == 0
 
 
 def test_status_strings(uz):

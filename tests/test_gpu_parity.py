@@ -222,8 +222,45 @@ def test_pipeline_send(mode):
                                sizes.data_ptr(), mode, s0.cuda_stream, s1.cuda_stream)
     assert st == 0, uz.uzip_status_string(st)
     torch.cuda.synchronize()
-    want = [oracle.compress(m) for m in msgs]
+    # messages under the default threshold travel as whole-message RAW
+    # containers (NCCLZ Sec. IV-C)
+    want = [oracle.compress(m, mode=oracle.MODE_RAW if 2 * m.size < uz.UZIP_PIPE_RAW_BELOW_DEFAULT else oracle.MODE_CHUNK)
+            for m in msgs]
     assert [int(v) for v in sizes] == [w.size for w in want]
     # banks now hold messages 2 (bank 0) and 1 (bank 1)
     for k, b in ((2, 0), (1, 1)):
         assert np.array_equal(hb[b].numpy()[: want[k].size], want[k])
+
+
+@pytest.mark.parametrize("mode", [0, 3, 4])
+def test_pipeline_send_ex_keeps_every_container(mode):
+    """uzip_pipeline_send_ex with one host bank per message: every container
+    stays on the host and equals the oracle's, coded (threshold 0) or, under
+    the threshold, whole-message RAW; each decodes back bit for bit."""
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+
+    msgs = [synth.normal_bf16((1 << 20) + 7 * k, 0.02, 19, k) for k in range(4)]
+    d_msgs = [gu.to_device(m) for m in msgs]
+    largest = max(m.size for m in msgs)
+    cap = uz.uzip_max_compressed_size(0, largest)
+    banks = [torch.empty(cap, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    hcap = cap + 16 * (-(-largest // 65536))
+    for raw_below, omode in ((0, oracle.MODE_CHUNK), (1 << 30, oracle.MODE_RAW)):
+        hb = [torch.zeros(hcap, dtype=torch.uint8).pin_memory() for _ in msgs]
+        sizes = torch.zeros(len(msgs), dtype=torch.int64).pin_memory()
+        s0, s1 = torch.cuda.Stream(), torch.cuda.Stream()
+        torch.cuda.synchronize()
+        st = uz.uzip_pipeline_send_ex(0, [t.data_ptr() for t in d_msgs], [m.size for m in msgs],
+                                      [b.data_ptr() for b in banks], cap, [h.data_ptr() for h in hb], hcap,
+                                      sizes.data_ptr(), mode, raw_below, s0.cuda_stream, s1.cuda_stream)
+        assert st == 0, uz.uzip_status_string(st)
+        torch.cuda.synchronize()
+        for k, m in enumerate(msgs):
+            want = oracle.compress(m, mode=omode)
+            assert int(sizes[k]) == want.size
+            got = hb[k].numpy()[: want.size]
+            assert np.array_equal(got, want)
+            back, status = gu.gpu_decompress(got, gu.BF16, m.size)
+            assert status == 0 and np.array_equal(back, m)
