@@ -93,9 +93,12 @@ typedef enum {
  * compressor's work area behind the largest frame.  In detail: the
  * largest possible container (every chunk stored RAW, rounded up to 16) plus
  * the compressor's work area behind it: 16 + 8*C bytes of counters and chunk
- * descriptors, 256 bytes of alignment slack and min(C, 1536) pairs of 68 KiB
- * slots (each compressing warp uses two, in turn, for a chunk's exponent bytes
- * and then for its finished stream while it waits for its offset).  Pure host function;
+ * descriptors, 4096 bytes of alignment slack and, for C > 0,
+ * min(ceil(C / 8), 160) blocks x 8 encoding warps x 2 slots of 69,632 bytes
+ * (each encoding warp uses its two slots in turn, for a chunk's exponent bytes
+ * and then for its finished stream while that waits for its offset).  For
+ * 2^29 bf16 values (C = 8192) that is 1,073,840,192 + 178,327,568 bytes.  Pure
+ * host function;
  * returns 0 for an unsupported dtype or n > UZIP_MAX_ELEMS. */
 uint64_t uzip_max_compressed_size(uzip_dtype dtype, uint64_t n);
 
@@ -162,8 +165,10 @@ uzip_status uzip_compress_ex(const void* d_in, uzip_dtype dtype, uint64_t n, voi
  * allocates nothing: it clears the work area with cudaMemsetAsync on s and
  * launches the same kernel.  The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture.  Every call shares the one array, so
- * two calls whose work overlaps on the GPU (different streams, or different
+ * first call before any stream capture.  The address is kept per device and
+ * CUDA context: after a cudaDeviceReset the next call on that device looks it
+ * up again (so that call too must come before any capture).  Every call
+ * shares the one array, so two calls whose work overlaps on the GPU (different streams, or different
  * host threads without ordering) race and corrupt each other's output: order
  * them on one stream or synchronise between them. */
 #define UZIP_NOALLOC_MAX_ELEMS (1ull << 30)
@@ -280,7 +285,7 @@ uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d_msgs, cons
  * whole-message RAW container (every chunk stored RAW, no statistics or
  * coding; NCCLZ Sec. IV-C: a message whose coding would not pay travels RAW):
  * below it, coding one message takes longer than copying its raw bytes. */
-#define UZIP_PIPE_RAW_BELOW_DEFAULT (32ull << 20)
+#define UZIP_PIPE_RAW_BELOW_DEFAULT (64ull << 20)
 
 /* The split-send pipeline with every choice explicit:
  *   h_bank[n_hbanks]  n_hbanks >= 2 pinned host banks; message k's container

@@ -1,6 +1,8 @@
 // Compressor host side: the launch entry points used by the C ABI and the
 // allocation-free work area.  The device code lives in compress_kernels.cuh
 // and is compiled once per element format (compress_fmt_*.cu).
+#include <cuda.h>
+
 #include <mutex>
 
 #include "compress_kernels.cuh"
@@ -73,25 +75,60 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchHead + 8 * (k
 
 namespace {
 std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+struct NoallocEntry {
+    unsigned long long ctx_id;  // CUDA context the address belongs to (0: unknown)
+    void* ptr;
+};
+NoallocEntry g_noalloc[kNoAllocMaxDevices] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Id of the current CUDA context (unique for the life of the process), or 0
+// if the driver cannot tell.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS) return id;
+    return 0;
+}
 }  // namespace
 
 // Device address of g_noalloc_scratch on the current device.  In host code
 // the array's name only stands in for the symbol, so the address is asked of
-// the runtime once per device (with that device current) and cached.
+// the runtime (with that device current) the first time a device is used and
+// kept; it is asked again when the device's CUDA context has changed since
+// (a cudaDeviceReset reloads the library's module, and the old address is
+// gone), which the context id tells.
 cudaError_t noalloc_scratch_address(void** ptr) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= int(kNoAllocMaxDevices)) return cudaErrorInvalidDevice;
+    const unsigned long long id = current_context_id();
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (g_noalloc_ptr[dev] == nullptr) {
+    NoallocEntry& e = g_noalloc[dev];
+    if (e.ptr == nullptr || e.ctx_id != id) {
         void* p = nullptr;
         err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (err != cudaSuccess) return err;
-        g_noalloc_ptr[dev] = p;
+        e.ptr = p;
+        e.ctx_id = id;
     }
-    *ptr = g_noalloc_ptr[dev];
+    *ptr = e.ptr;
     return cudaSuccess;
 }
 

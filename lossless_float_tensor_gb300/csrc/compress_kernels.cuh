@@ -1204,8 +1204,12 @@ __global__ void __launch_bounds__(32) gate_kernel(CompressArgs a, uint32_t n_s) 
 }
 
 // raw_kernel: every chunk RAW.  Offsets need no look-back: chunk c's RAW
-// stream (its exponent bytes) starts at 65536 c of the exponent section.
+// stream (its exponent bytes) starts at 65536 c of the exponent section.  The
+// work is cut into pieces of kRawPiece elements, one warp each, so that a
+// message of a few chunks still spreads over the GPU (the remainder fields of
+// a piece start on a byte: kRawPiece * W / 8 is whole for every format).
 // Exits at once when a gate ran and chose coding.
+constexpr uint32_t kRawPiece = 4096;
 template <int DT>
 __global__ void __launch_bounds__(32) raw_kernel(CompressArgs a) {
     if (a.gated && *reinterpret_cast<volatile uint32_t*>(&a.scratch->pad) == 0) return;
@@ -1213,20 +1217,27 @@ __global__ void __launch_bounds__(32) raw_kernel(CompressArgs a) {
     const uint64_t n = a.n, C = a.num_chunks;
     const uint64_t rem_off = rem_offset(n), exp_off = exp_offset(DT, n);
     const uint64_t pol = policy_evict_first();
-    for (uint64_t c = blockIdx.x; c < C; c += gridDim.x) {
+    constexpr uint32_t kPer = kChunk / kRawPiece;  // pieces per chunk
+    const uint64_t P = (n + kRawPiece - 1) / kRawPiece;
+    for (uint64_t p = blockIdx.x; p < P; p += gridDim.x) {
+        const uint64_t c = p / kPer, sub = p % kPer;
         const uint64_t left = n - c * kChunk;
         const uint32_t n_c = uint32_t(left < kChunk ? left : kChunk);
-        const uint8_t* cin = a.in + c * kChunk * Fmt<DT>::kEs;
+        const uint32_t first = uint32_t(sub) * kRawPiece;
+        const uint32_t n_p = n_c - first < kRawPiece ? n_c - first : kRawPiece;
+        const uint8_t* cin = a.in + (c * kChunk + first) * Fmt<DT>::kEs;
+        uint8_t* rem = a.out + rem_off + c * Fmt<DT>::kRemChunk + uint64_t(first) / 8 * Fmt<DT>::kRbits;
         uint8_t* dst = a.out + exp_off + c * kChunk;
         if constexpr (Fmt<DT>::kPacked)
-            split_and_count_packed<DT, 0>(cin, n_c, a.out + rem_off + c * Fmt<DT>::kRemChunk, dst, nullptr, lane,
-                                              pol);
+            split_and_count_packed<DT, 0>(cin, n_p, rem, dst + first, nullptr, lane, pol);
         else
-            split_and_count<DT, 0>(cin, n_c, a.out + rem_off + c * Fmt<DT>::kRemChunk, dst, nullptr, lane, pol);
-        for (uint32_t i = n_c + lane; i < round16(n_c); i += 32) dst[i] = 0;
-        if (lane == 0) {
-            reinterpret_cast<uint64_t*>(a.out + kHeader)[c] = c * kChunk;
-            reinterpret_cast<uint32_t*>(a.out + kHeader + 8 * C)[c] = n_c | kRawFlag;
+            split_and_count<DT, 0>(cin, n_p, rem, dst + first, nullptr, lane, pol);
+        if (first + n_p == n_c) {  // the chunk's last piece: padding and table entries
+            for (uint32_t i = n_c + lane; i < round16(n_c); i += 32) dst[i] = 0;
+            if (lane == 0) {
+                reinterpret_cast<uint64_t*>(a.out + kHeader)[c] = c * kChunk;
+                reinterpret_cast<uint32_t*>(a.out + kHeader + 8 * C)[c] = n_c | kRawFlag;
+            }
         }
     }
     if (blockIdx.x == 0 && lane == 0) write_header<DT>(a, container_bound(DT, n), 0);
@@ -1259,7 +1270,8 @@ cudaError_t launch_mode(CompressArgs a, int mode, bool stash, cudaStream_t s) {
         if ((err = launch_shape(reinterpret_cast<const void*>(raw_kernel<DT>), 32, 0, &sms, &per_sm)) != cudaSuccess)
             return err;
         uint64_t grid = uint64_t(per_sm) * uint64_t(sms);
-        if (grid > C) grid = C;
+        const uint64_t pieces = (n + kRawPiece - 1) / kRawPiece;
+        if (grid > pieces) grid = pieces;
         if (grid < 1) grid = 1;
         raw_kernel<DT><<<dim3(uint32_t(grid)), dim3(32), 0, s>>>(a);
         if ((err = cudaGetLastError()) != cudaSuccess || mode == 1) return err;

@@ -142,7 +142,8 @@ def test_pipeline_send_sized(code):
                                s0.cuda_stream, s1.cuda_stream)
     assert st == 0, uz.uzip_status_string(st)
     torch.cuda.synchronize()
-    for k, m in enumerate(msgs):
-        want = oracle.compress(m, code)
+    for k, m in enumerate(msgs):  # under the default threshold: whole-message RAW
+        mode = oracle.MODE_RAW if m.nbytes < uz.UZIP_PIPE_RAW_BELOW_DEFAULT else oracle.MODE_CHUNK
+        want = oracle.compress(m, code, mode=mode)
         assert int(sizes[k]) == want.size
         assert np.array_equal(hb[k % 2].numpy()[: want.size], want)
