@@ -30,14 +30,22 @@ sys.path.insert(0, ROOT)
 METRIC = "compress & decompress GB/s (input bytes), ratio, % of HBM roofline, 1 GB300"
 WORKLOAD = ("c4: bf16 activations [8, 8192, 8192] ~ 0.5*Student-t(4), 82 outlier channels x50, "
             "chunk 4096 random bits; 536,870,912 values (1 GiB)")
-KERNEL_SOURCES = ["lossless_float_tensor_gb300/csrc/compress_kernels.cuh", "lossless_float_tensor_gb300/csrc/compress_ws.cuh",
-                  "lossless_float_tensor_gb300/csrc/compress.cu", "lossless_float_tensor_gb300/csrc/decompress.cu",
-                  "lossless_float_tensor_gb300/csrc/uzip_internal.cuh"]
+_CSRC = "lossless_float_tensor_gb300/csrc/"
+# Sources each kernel is compiled from; a committed DRAM-traffic figure is
+# only used while the hash of its kernel's sources is unchanged.
+KERNEL_SOURCES = {
+    "compress": [_CSRC + f for f in ("compress_kernels.cuh", "compress_ws.cuh", "compress.cu", "compress_fmt_bf16.cu",
+                                     "uzip_internal.cuh")],
+    "decompress": [_CSRC + f for f in ("decompress.cu", "uzip_internal.cuh")],
+}
 
 
-def kernel_hash() -> str:
+def kernel_hash(kernel: str | None = None) -> str:
+    """16 hex digits of sha256 over one kernel's sources (all sources when
+    kernel is None)."""
+    files = KERNEL_SOURCES[kernel] if kernel else sorted({f for v in KERNEL_SOURCES.values() for f in v})
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in files:
         with open(os.path.join(ROOT, p), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -60,7 +68,7 @@ def profiled_traffic(kernel: str):
     with open(p) as fh:
         d = json.load(fh)
     e = d.get(kernel)
-    if not e or e.get("source_hash") != kernel_hash():
+    if not e or kernel not in KERNEL_SOURCES or e.get("source_hash") != kernel_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch_full")
 
@@ -436,6 +444,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk.summary(), "e2e": e2e, "gpu_launches": 2 * args.steps,
         "wall_s_timed_region": wall, "cpu_baseline": cpu, "configs": configs, "pipeline": pipe,
         "dtype_sweep": sweep, "gate": gate, "kernel_source_hash": kernel_hash(),
+        "kernel_source_hashes": {k: kernel_hash(k) for k in KERNEL_SOURCES},
     }
     return line
 

@@ -15,22 +15,24 @@ def _committed():
 
 
 def test_kernel_hash_is_stable_hex():
-    h = bench.kernel_hash()
-    assert h == bench.kernel_hash()
-    assert len(h) == 16 and int(h, 16) >= 0
+    for k in (None, "compress", "decompress"):
+        h = bench.kernel_hash(k)
+        assert h == bench.kernel_hash(k)
+        assert len(h) == 16 and int(h, 16) >= 0
+    assert bench.kernel_hash("compress") != bench.kernel_hash("decompress")
 
 
 @pytest.mark.parametrize("kernel", ["compress", "decompress"])
 def test_traffic_only_for_the_captured_sources(kernel, monkeypatch):
     entry = _committed()[kernel]
-    monkeypatch.setattr(bench, "kernel_hash", lambda: entry["source_hash"])
+    monkeypatch.setattr(bench, "kernel_hash", lambda k=None: entry["source_hash"])
     got = bench.profiled_traffic(kernel)
     assert got == entry["dram_bytes_per_launch_full"]
     # scaled from the capture by the chunk counts of the two launches
     small = entry["dram_bytes_read_small"] + entry["dram_bytes_write_small"]
     chunks = lambda n: -(-n // 65536)  # noqa: E731
     assert got == pytest.approx(small * chunks(entry["elements_full"]) / chunks(entry["elements_small"]))
-    monkeypatch.setattr(bench, "kernel_hash", lambda: "0" * 16)
+    monkeypatch.setattr(bench, "kernel_hash", lambda k=None: "0" * 16)
     assert bench.profiled_traffic(kernel) is None
 
 
