@@ -94,7 +94,7 @@ typedef enum {
  * largest possible container (every chunk stored RAW, rounded up to 16) plus
  * the compressor's work area behind it: 16 + 8*C bytes of counters and chunk
  * descriptors, 4096 bytes of alignment slack and, for C > 0,
- * min(ceil(C / 8), 160) blocks x 8 encoding warps x 2 slots of 69,632 bytes
+ * min(ceil(C / 4), 160) blocks x 8 encoding warps x 2 slots of 69,632 bytes
  * (each encoding warp uses its two slots in turn, for a chunk's exponent bytes
  * and then for its finished stream while that waits for its offset).  For
  * 2^29 bf16 values (C = 8192) that is 1,073,840,192 + 178,327,568 bytes.  Pure
@@ -251,7 +251,9 @@ const char* uzip_status_string(uzip_status st);
  *                            issues one cudaMemcpyAsync of exactly that many
  *                            bytes (the copy engine instead of SM stores; the
  *                            call then blocks until the last compression has
- *                            finished, while the copies still overlap it).
+ *                            finished, while the copies still overlap it).  A
+ *                            whole-message RAW container's size is the bound,
+ *                            known up front, so its copy is issued at once.
  *                            UZIP_PIPE_STREAMED: each message's container
  *                            travels while it is being compressed (UCCL-Zip
  *                            Fig. 4 d, split-send at plane and chunk grain):
@@ -285,7 +287,7 @@ uzip_status uzip_pipeline_send(uzip_dtype dtype, const void* const* d_msgs, cons
  * whole-message RAW container (every chunk stored RAW, no statistics or
  * coding; NCCLZ Sec. IV-C: a message whose coding would not pay travels RAW):
  * below it, coding one message takes longer than copying its raw bytes. */
-#define UZIP_PIPE_RAW_BELOW_DEFAULT (64ull << 20)
+#define UZIP_PIPE_RAW_BELOW_DEFAULT (32ull << 20)
 
 /* The split-send pipeline with every choice explicit:
  *   h_bank[n_hbanks]  n_hbanks >= 2 pinned host banks; message k's container

@@ -29,7 +29,7 @@ UZIP_NOALLOC_MAX_ELEMS = 1 << 30
 UZIP_TESTFLAG_SKIP_CHUNK0 = 1
 UZIP_FLAG_SAMPLED_TABLES = 2
 UZIP_PIPE_EXACT, UZIP_PIPE_BOUND, UZIP_PIPE_SERIAL, UZIP_PIPE_SIZED, UZIP_PIPE_STREAMED = 0, 1, 2, 3, 4
-UZIP_PIPE_RAW_BELOW_DEFAULT = 64 << 20
+UZIP_PIPE_RAW_BELOW_DEFAULT = 32 << 20
 UZIP_MAX_ELEMS = 1 << 40
 CHUNK_ELEMS = 65536
 HEADER_BYTES = 64

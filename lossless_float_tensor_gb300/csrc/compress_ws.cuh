@@ -808,7 +808,7 @@ cudaError_t launch_ws(const CompressArgs& a, cudaStream_t s) {
         return err;
     const uint64_t work = a.num_chunks - a.first_ticket;
     uint64_t grid = uint64_t(sms) * uint64_t(per_sm);
-    const uint64_t need = (work + kWsEnc - 1) / kWsEnc;
+    const uint64_t need = (work + kWsFirst - 1) / kWsFirst;
     if (grid > need) grid = need;
     if (grid > ws_ctas(a.n)) grid = ws_ctas(a.n);  // contexts in the slot area
     if (grid < 1) grid = 1;

@@ -194,7 +194,9 @@ extern "C" uzip_status uzip_pipeline_send_ex(uzip_dtype dtype, const void* const
         if (mk == UZIP_PIPE_STREAMED) {
             err = stream_out(dtype, msg_elems[k], static_cast<const uint8_t*>(d_bank[b]), static_cast<uint8_t*>(hb),
                              prog_off, compressed[b], sx);
-        } else if (mk == UZIP_PIPE_BOUND) {
+        } else if (mk == UZIP_PIPE_BOUND || (mk == UZIP_PIPE_SIZED && raw_msg)) {
+            // a whole-message RAW container is exactly the bound: its size is
+            // known on the host without waiting for the compression
             err = cudaMemcpyAsync(hb, d_bank[b], container_bound(dtype, msg_elems[k]), cudaMemcpyDeviceToHost, sx);
         } else if (mk == UZIP_PIPE_SIZED) {
             // the size is known once this compression is done; message k-1's

@@ -98,10 +98,15 @@ __host__ __device__ inline uint64_t scratch_bytes(uint64_t n) { return kScratchH
 // slots (contexts), used in turn; the one-warp compressor (sampled tables)
 // gives each warp two.  Slots are never read before they are written.
 constexpr uint32_t kWsEnc = 8;                   // encoder warps per block of the warp-specialised compressor
+constexpr uint32_t kWsFirst = kWsEnc / 2;        // chunks a block starts on at once: one per helper warp
 constexpr uint64_t kWsMaxCtas = 160;             // blocks the slot area is sized for
 constexpr uint32_t kSlotBytes = 65536 + 4096;
+// Blocks of the warp-specialised compressor for n values: one per kWsFirst
+// chunks (a helper splits its two encoders' first chunks one after the
+// other, so a small tensor spread over more blocks starts every chunk at
+// once), at most kWsMaxCtas.
 __host__ __device__ inline uint64_t ws_ctas(uint64_t n) {
-    const uint64_t c = (num_chunks(n) + kWsEnc - 1) / kWsEnc;
+    const uint64_t c = (num_chunks(n) + kWsFirst - 1) / kWsFirst;
     return c < kWsMaxCtas ? c : kWsMaxCtas;
 }
 __host__ __device__ inline uint64_t slot_area_bytes(uint64_t n) { return ws_ctas(n) * kWsEnc * 2 * uint64_t(kSlotBytes); }

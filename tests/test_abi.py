@@ -43,14 +43,15 @@ def test_exports_every_declared_symbol(uz):
 
 def test_max_compressed_size_is_container_bound_plus_work_area(uz):
     for dtype in range(5):  # bf16, fp32, fp16, fp8 e4m3fn, fp8 e5m2
-        for n in [0, 1, 15, 16, 17, 65535, 65536, 65537, 3 * 65536 + 5, 1 << 29]:
+        for n in [0, 1, 15, 16, 17, 65535, 65536, 65537, 3 * 65536 + 5, 5 * 65536, 700 * 65536 - 3, 1 << 29]:
             c = -(-n // 65536)
             bound = oracle.container_bound(dtype, n)
             off = uz.library().uzip_debug_scratch_offset(dtype, n)
             assert off == -(-bound // 16) * 16
             # counters and descriptors, 4 KiB of alignment slack, and two
-            # 68 KiB slots for each of the 8 encoders of up to 160 blocks
-            work = 16 + 8 * c + 4096 + min(-(-c // 8), 160) * 8 * 2 * 69632
+            # 68 KiB slots for each of the 8 encoders of one block per 4
+            # chunks, at most 160 blocks
+            work = 16 + 8 * c + 4096 + min(-(-c // 4), 160) * 8 * 2 * 69632
             assert uz.uzip_max_compressed_size(dtype, n) == off + work
     assert uz.uzip_max_compressed_size(7, 10) == 0
     assert uz.uzip_max_compressed_size(0, (1 << 40) + 1) == 0
@@ -142,3 +143,20 @@ def test_package_refuses_to_import_without_the_library(monkeypatch):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError, match="not built"):
         spec.loader.exec_module(mod)
+
+
+def test_binding_constants_match_the_header(uz):
+    """The Python binding repeats the header's #define and enum values."""
+    text = open(os.path.join(ROOT, "include", "uzip.h")).read()
+    defines = {m.group(1): m.group(2) for m in re.finditer(r"#define\s+(UZIP_[A-Z0-9_]+)\s+(.+)", text)}
+    for name, expr in defines.items():
+        if not hasattr(uz, name):
+            continue
+        expr = re.sub(r"(\d+)[uUlL]*", r"\1", expr.split("/*")[0]).strip()
+        assert re.fullmatch(r"[\d\s()<]+", expr), expr
+        value = eval(expr, {"__builtins__": {}})
+        assert getattr(uz, name) == value, name
+    assert uz.UZIP_PIPE_RAW_BELOW_DEFAULT == 32 << 20
+    for name, value in re.findall(r"\b(UZIP_[A-Z0-9_]+)\s*=\s*(\d+)", text):
+        if hasattr(uz, name):
+            assert getattr(uz, name) == int(value), name
