@@ -673,7 +673,14 @@ __device__ void ws_encode(const CompressArgs& a, uint8_t* team, uint32_t cx, uin
             break;
         }
         ring_ph ^= 1u << rs;
-        if (b + 1 <= bt && lane < 8) l2_discard_line(ctx + 1024 * uint32_t(b + 1) + 128 * lane);  // read back: spent
+        // block b + 1 has been read back; its lines are dropped from L2 unless
+        // flushed words may already sit in them (a stream that grows faster
+        // than 8 bits a value reaches the block just read: words above
+        // `flushed` are in the context, and a discarded line loses them)
+        if (b + 1 <= bt && lane < 8) {
+            const uint32_t line = 1024 * uint32_t(b + 1) + 128 * lane;
+            if (line + 128 <= flushed) l2_discard_line(ctx + line);
+        }
         if (b >= 3) {  // block b - 3 goes into the slot block b + 1 has left (its reads are done)
             warp_sync_asm();
             issue(b - 3);

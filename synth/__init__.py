@@ -352,3 +352,53 @@ def normal_fp32(n: int, std: float = 0.02, cfg: int = 12, tensor: int = 0, start
         return (normal(key, idx, 2, 0) * std).astype(np.float32).view(np.uint32)
 
     return _parallel_fill(np.empty(n, np.uint32), n, fn)
+
+
+# --------------------------------------------------------------------------
+# chunks whose coded stream grows faster than their exponent bytes are read
+# (a coder runs a chunk from its last value down, so what sits at the top of
+# a chunk is coded first)
+
+GROWTH_RANDOM_TOPS = (0.46, 0.48, 0.50, 0.52, 0.55, 0.60)
+GROWTH_RARE_COUNTS = (64, 80, 94, 110, 128)
+
+
+def growth_exponents(tail: int = 4097) -> np.ndarray:
+    """8-bit exponent fields, chunk by chunk (65536 values each).
+
+    Chunk k < 6: exponent 127 below, uniformly random exponents in the top
+    fraction GROWTH_RANDOM_TOPS[k].  Chunk 6 + j: the 255 exponents other than
+    127, GROWTH_RARE_COUNTS[j] times each in a shuffled order, at the top; 127
+    below.  Then `tail` values of exponent 126 or 127 (a partial chunk)."""
+    chunks = []
+    for k, p in enumerate(GROWTH_RANDOM_TOPS):
+        key = stream_key(13, k)
+        top = int(round(p * 65536))
+        e = np.full(65536, 127, np.uint8)
+        e[65536 - top:] = (raw64(key, np.arange(top, dtype=np.uint64), 1, 0) & np.uint64(0xFF)).astype(np.uint8)
+        chunks.append(e)
+    others = np.array([s for s in range(256) if s != 127], np.uint8)
+    for j, c in enumerate(GROWTH_RARE_COUNTS):
+        key = stream_key(13, 100 + j)
+        top = np.repeat(others, c)
+        order = np.argsort(raw64(key, np.arange(top.size, dtype=np.uint64), 1, 0), kind="stable")
+        e = np.full(65536, 127, np.uint8)
+        e[65536 - top.size:] = top[order]
+        chunks.append(e)
+    key = stream_key(13, 200)
+    chunks.append((126 + (raw64(key, np.arange(tail, dtype=np.uint64), 1, 0) & np.uint64(1))).astype(np.uint8))
+    return np.concatenate(chunks)
+
+
+def growth_bf16(tail: int = 4097) -> np.ndarray:
+    """bf16 bit patterns with growth_exponents() and random sign and fraction."""
+    e = growth_exponents(tail).astype(np.uint16)
+    r = raw64(stream_key(13, 300), np.arange(e.size, dtype=np.uint64), 1, 0)
+    return ((e << np.uint16(7)) | (r & np.uint64(0x807F)).astype(np.uint16)).astype(np.uint16)
+
+
+def growth_fp32(tail: int = 4097) -> np.ndarray:
+    """fp32 bit patterns with growth_exponents() and random sign and fraction."""
+    e = growth_exponents(tail).astype(np.uint32)
+    r = raw64(stream_key(13, 301), np.arange(e.size, dtype=np.uint64), 1, 0)
+    return ((e << np.uint32(23)) | (r & np.uint64(0x807FFFFF)).astype(np.uint32)).astype(np.uint32)

@@ -100,6 +100,22 @@ def test_chunks_whose_tail_outgrows_the_slot():
     assert not (lens[1] & 0x80000000)
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "fp32"])
+def test_streams_growing_faster_than_their_exponents_are_read(fmt):
+    """Chunks whose top part (coded first) costs more than 8 bits a value:
+    random exponents over a constant run (six fractions), and the 255 rarer
+    exponents 64 to 128 times each over a constant run.  The words written
+    from the slot's end reach the 1 KiB block of exponent bytes just read
+    (all of them) or would pass blocks still to be read (80, 94 and 110 per
+    exponent, which then code from the input); every chunk stays coded."""
+    bits = synth.growth_bf16() if fmt == "bf16" else synth.growth_fp32()
+    comp = _parity(bits)
+    c = -(-bits.size // 65536)
+    lens = comp[64 + 8 * c:64 + 12 * c].view(np.uint32)
+    assert not np.any(lens & 0x80000000)
+    assert np.all(lens[:11] > 20000)
+
+
 def test_all_bf16_patterns_and_fp32_specials():
     x = np.arange(65536 * 3, dtype=np.uint32).astype(np.uint16)
     _parity(x)
