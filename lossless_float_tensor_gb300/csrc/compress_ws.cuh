@@ -44,7 +44,11 @@ namespace uzip {
 constexpr uint32_t kWsHelp = kWsEnc / 2;
 constexpr uint32_t kWsRing = 4096;
 constexpr uint32_t kWsWordRing = 4096;
-constexpr uint32_t kWsTables = 8192;
+constexpr uint32_t kWsTables = kWsRing + kWsWordRing;
+constexpr uint32_t kWsFlushAt = 2032;  // unflushed word bytes that start a flush
+// a block writes at most 2 KiB of words; with no flush pending the ring must
+// hold them beside the words not yet flushed (under kWsFlushAt + 16 bytes)
+static_assert(kWsFlushAt + 16 + 2048 <= kWsWordRing, "word ring too small for the flush threshold");
 constexpr uint32_t kWsTableBytes = 2048;  // one context's table
 constexpr uint32_t kWsMeta = kWsTables + 2 * kWsTableBytes;
 constexpr uint32_t kWsMetaBytes = 576;
@@ -645,12 +649,13 @@ __device__ void ws_encode(const CompressArgs& a, uint8_t* team, uint32_t cx, uin
     };
     for (int32_t i = 0; i < 3 && bt - i >= 0; ++i) issue(bt - i);
     int32_t issued_lo = bt - 2 > 0 ? bt - 2 : 0;  // lowest block issued
-    WsEnc st{kRansL, kSlotBytes, smem_u32(team + kWsWordRing), lanemask_lt(), smem_u32(team + kWsProgress + 4)};
-    uint32_t flushed = kSlotBytes;  // context bytes at and above this offset hold flushed words
-    uint32_t prev_emit = 0;
+    WsEnc st{kRansL, kSlotBytes, smem_u32(team + kWsRing), lanemask_lt(), smem_u32(team + kWsProgress + 4)};
+    uint32_t flushed = kSlotBytes;  // context bytes at and above this offset hold flushed (or flushing) words
+    uint32_t pend = 0;              // bytes of the last flush, whose reads of the ring may not be done
     bool raw = false, err = false, slow = false;
     auto flush = [&](uint32_t lo) {  // ring lines [lo, flushed) to the context
         warp_sync_asm();
+        pend = flushed > lo ? flushed - lo : 0u;
         if (lane == 0 && lo < flushed) {
             fence_async_shared();
             for (uint32_t p = lo; p < flushed;) {
@@ -676,7 +681,10 @@ __device__ void ws_encode(const CompressArgs& a, uint8_t* team, uint32_t cx, uin
         // block b + 1 has been read back; its lines are dropped from L2 unless
         // flushed words may already sit in them (a stream that grows faster
         // than 8 bits a value reaches the block just read: words above
-        // `flushed` are in the context, and a discarded line loses them)
+        // `flushed` are in the context, and a discarded line loses them).  A
+        // later flush may write a dropped line again; it is issued at the end
+        // of a block, thousands of cycles after the drop, which reaches L2
+        // first.
         if (b + 1 <= bt && lane < 8) {
             const uint32_t line = 1024 * uint32_t(b + 1) + 128 * lane;
             if (line + 128 <= flushed) l2_discard_line(ctx + line);
@@ -686,14 +694,18 @@ __device__ void ws_encode(const CompressArgs& a, uint8_t* team, uint32_t cx, uin
             issue(b - 3);
             issued_lo = b - 3;
         }
-        // the word ring: lines this block may write were flushed at most two
-        // blocks ago (one, if the last block wrote more than 1 KiB)
+        // the word ring holds the last flush while its reads are pending
+        // (pend bytes, above `flushed`), the words not yet flushed (under
+        // kWsFlushAt + 16) and this block's words (at most 2 KiB): every
+        // earlier flush must have been read, and the last one too unless all
+        // three fit (with kWsFlushAt <= 2032 the last two always do)
+        const bool fits = pend + (flushed - st.dp) + 2048 <= kWsWordRing;
         if (lane == 0) {
-            if (prev_emit > 1024) bulk_wait_read<0>();
-            else bulk_wait_read<1>();
+            if (fits) bulk_wait_read<1>();
+            else bulk_wait_read<0>();
         }
+        if (!fits) pend = 0;
         warp_sync_asm();
-        const uint32_t dp0 = st.dp;
         const uint32_t ex0 = opaque(ring_s + rs * 1024 + lane);  // valid once block b's wait is over
         if (b == bt && partial_top) {
             for (int32_t t = T - 1; t >= 32 * b; --t)
@@ -701,7 +713,6 @@ __device__ void ws_encode(const CompressArgs& a, uint8_t* team, uint32_t cx, uin
         } else {
             ws_block(st, ex0, table_s);
         }
-        prev_emit = dp0 - st.dp;
         if (hdr + (kSlotBytes - st.dp) >= n_c) {  // coding does not pay: RAW
             raw = true;
             break;
@@ -711,7 +722,7 @@ __device__ void ws_encode(const CompressArgs& a, uint8_t* team, uint32_t cx, uin
             slow = true;
             break;
         }
-        flush(lo);
+        if (flushed - lo >= kWsFlushAt) flush(lo);  // fewer, larger flushes: each costs a proxy fence
     }
     // ring blocks issued but not waited for (a chunk cut short) complete first
     for (int32_t bb = (err ? b : b - 1); bb >= issued_lo && bb >= 0; --bb) {
