@@ -23,15 +23,18 @@ extern template cudaError_t launch_mode<UZIP_FP8_E5M2>(CompressArgs, int, bool, 
 
 // Launches the compressor with its work area (status, ticket, done counter,
 // look-back descriptors: scratch_bytes(n) bytes) at `scratch`, which is
-// zeroed on `s` first.
+// zeroed on `s` first (mode 1, whole-message RAW, needs no work area: only
+// the container's bytes of d_out are written).
 cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                                          int32_t* d_status, uint32_t first_ticket, void* scratch_area, void* stash,
                                          cudaStream_t s, int mode, uint64_t* progress) {
     const uint64_t C = num_chunks(n);
     uint8_t* out = static_cast<uint8_t*>(d_out);
     Scratch* scratch = static_cast<Scratch*>(scratch_area);
-    cudaError_t err = cudaMemsetAsync(scratch, 0, scratch_bytes(n), s);
-    if (err != cudaSuccess) return err;
+    if (mode != 1) {  // the whole-message RAW kernel uses no work area
+        const cudaError_t err = cudaMemsetAsync(scratch, 0, scratch_bytes(n), s);
+        if (err != cudaSuccess) return err;
+    }
     CompressArgs a;
     a.in = static_cast<const uint8_t*>(d_in);
     a.n = n;

@@ -133,25 +133,45 @@ extern "C" uzip_status uzip_pipeline_send_ex(uzip_dtype dtype, const void* const
     const bool serial = mode == UZIP_PIPE_SERIAL;
     cudaStream_t sc = s_compress;
     cudaStream_t sx = serial ? s_compress : s_copy;
-    cudaEvent_t compressed[2] = {nullptr, nullptr}, copied[2] = {nullptr, nullptr};
+    // whole-message RAW below the threshold (NCCLZ Sec. IV-C: a message whose
+    // coding does not pay travels RAW).  A RAW container needs only its own
+    // bytes in a device bank, so when every message travels RAW each bank
+    // holds up to kSubSlots of them and up to 2 kSubSlots messages are in
+    // flight instead of two (small messages are bound by the latency of the
+    // hand-over between the streams, not by the copy engine).
+    constexpr uint32_t kSubSlots = 8;
+    bool all_raw = true;
+    uint64_t raw_need = 0;
+    for (uint32_t k = 0; k < n_msgs; ++k) {
+        if (msg_elems[k] * elem_bytes(dtype) >= raw_below_bytes) all_raw = false;
+        const uint64_t need = (container_bound(dtype, msg_elems[k]) + 255) & ~uint64_t(255);
+        if (need > raw_need) raw_need = need;
+    }
+    uint32_t sub = 1;
+    if (all_raw && !serial && raw_need > 0) {
+        const uint64_t fit = bank_capacity / raw_need;
+        sub = fit < kSubSlots ? uint32_t(fit) : kSubSlots;
+        if (sub < 1) sub = 1;
+    }
+    const uint32_t nslots = 2 * sub;  // slot v: bank v % 2, at (v / 2) * raw_need in it
+    cudaEvent_t compressed[2 * kSubSlots] = {}, copied[2 * kSubSlots] = {};
     uzip_status result = UZIP_OK;
-    for (int b = 0; b < 2 && result == UZIP_OK; ++b) {
-        if (cudaEventCreateWithFlags(&compressed[b], cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&copied[b], cudaEventDisableTiming) != cudaSuccess)
+    for (uint32_t v = 0; v < nslots && result == UZIP_OK; ++v) {
+        if (cudaEventCreateWithFlags(&compressed[v], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&copied[v], cudaEventDisableTiming) != cudaSuccess)
             result = UZIP_ERR_CUDA;
     }
     for (uint32_t k = 0; k < n_msgs && result == UZIP_OK; ++k) {
-        const int b = int(k & 1u);          // device bank
+        const uint32_t b = k % nslots;      // device slot
+        void* dbank = static_cast<uint8_t*>(d_bank[b % 2]) + uint64_t(b / 2) * raw_need;
         void* hb = h_bank[k % n_hbanks];    // host bank
         void* hd = nullptr;                 // its device-side address
         host_mapped(hb, &hd);
-        // whole-message RAW below the threshold (NCCLZ Sec. IV-C: a message
-        // whose coding does not pay travels RAW); such a message is copied
-        // with the sized scheme when the streamed one is asked for
+        // a RAW message asked to stream is copied with the sized scheme
         const bool raw_msg = msg_elems[k] * elem_bytes(dtype) < raw_below_bytes;
         const uzip_pipe_mode mk = (raw_msg && mode == UZIP_PIPE_STREAMED) ? UZIP_PIPE_SIZED : mode;
-        // bank b still holds message k-2 until its copy has finished
-        if (k >= 2 && !serial && cudaStreamWaitEvent(sc, copied[b], 0) != cudaSuccess) {
+        // slot b still holds message k - nslots until its copy has finished
+        if (k >= nslots && !serial && cudaStreamWaitEvent(sc, copied[b], 0) != cudaSuccess) {
             result = UZIP_ERR_CUDA;
             break;
         }
@@ -160,7 +180,7 @@ extern "C" uzip_status uzip_pipeline_send_ex(uzip_dtype dtype, const void* const
                 result = UZIP_ERR_INVALID_ARG;
                 break;
             }
-            if (launch_compress(dtype, d_msgs[k], msg_elems[k], d_bank[b], static_cast<uint64_t*>(sizes_dev) + k, nullptr,
+            if (launch_compress(dtype, d_msgs[k], msg_elems[k], dbank, static_cast<uint64_t*>(sizes_dev) + k, nullptr,
                                 0, sc, 1) != cudaSuccess) {
                 result = UZIP_ERR_CUDA;
                 break;
@@ -174,13 +194,13 @@ extern "C" uzip_status uzip_pipeline_send_ex(uzip_dtype dtype, const void* const
                 break;
             }
             uint64_t* prog_dev = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(hd) + prog_off);
-            if (launch_compress(dtype, d_msgs[k], msg_elems[k], d_bank[b], static_cast<uint64_t*>(sizes_dev) + k, nullptr,
+            if (launch_compress(dtype, d_msgs[k], msg_elems[k], dbank, static_cast<uint64_t*>(sizes_dev) + k, nullptr,
                                 0, sc, 0, prog_dev) != cudaSuccess) {
                 result = UZIP_ERR_CUDA;
                 break;
             }
         } else {
-            result = uzip_compress(d_msgs[k], dtype, msg_elems[k], d_bank[b], bank_capacity,
+            result = uzip_compress(d_msgs[k], dtype, msg_elems[k], dbank, bank_capacity,
                                    static_cast<uint64_t*>(sizes_dev) + k, sc);
             if (result != UZIP_OK) break;
         }
@@ -192,28 +212,28 @@ extern "C" uzip_status uzip_pipeline_send_ex(uzip_dtype dtype, const void* const
         }
         cudaError_t err = cudaSuccess;
         if (mk == UZIP_PIPE_STREAMED) {
-            err = stream_out(dtype, msg_elems[k], static_cast<const uint8_t*>(d_bank[b]), static_cast<uint8_t*>(hb),
+            err = stream_out(dtype, msg_elems[k], static_cast<const uint8_t*>(dbank), static_cast<uint8_t*>(hb),
                              prog_off, compressed[b], sx);
         } else if (mk == UZIP_PIPE_BOUND || (mk == UZIP_PIPE_SIZED && raw_msg)) {
             // a whole-message RAW container is exactly the bound: its size is
             // known on the host without waiting for the compression
-            err = cudaMemcpyAsync(hb, d_bank[b], container_bound(dtype, msg_elems[k]), cudaMemcpyDeviceToHost, sx);
+            err = cudaMemcpyAsync(hb, dbank, container_bound(dtype, msg_elems[k]), cudaMemcpyDeviceToHost, sx);
         } else if (mk == UZIP_PIPE_SIZED) {
             // the size is known once this compression is done; message k-1's
             // copy keeps running on s_copy meanwhile
             err = cudaEventSynchronize(compressed[b]);
             const uint64_t total = *reinterpret_cast<volatile const uint64_t*>(h_sizes + k);
             if (err == cudaSuccess && total > 0)
-                err = cudaMemcpyAsync(hb, d_bank[b], total, cudaMemcpyDeviceToHost, sx);
+                err = cudaMemcpyAsync(hb, dbank, total, cudaMemcpyDeviceToHost, sx);
         } else {
-            err = launch_copy_exact(d_bank[b], hd, sx);
+            err = launch_copy_exact(dbank, hd, sx);
         }
         if (err == cudaSuccess && !serial) err = cudaEventRecord(copied[b], sx);
         if (err != cudaSuccess) result = UZIP_ERR_CUDA;
     }
-    for (int b = 0; b < 2; ++b) {
-        if (compressed[b]) cudaEventDestroy(compressed[b]);
-        if (copied[b]) cudaEventDestroy(copied[b]);
+    for (uint32_t v = 0; v < 2 * kSubSlots; ++v) {
+        if (compressed[v]) cudaEventDestroy(compressed[v]);
+        if (copied[v]) cudaEventDestroy(copied[v]);
     }
     if (result == UZIP_ERR_CUDA) cudaGetLastError();
     return result;
