@@ -229,6 +229,10 @@ const char* uzip_status_string(uzip_status st);
  *   d_msgs[k], msg_elems[k]  device input of message k (16-byte aligned).
  *   d_bank[2]                device banks, each bank_capacity bytes, at least
  *                            uzip_max_compressed_size of the largest message.
+ *                            When every message travels RAW (below the
+ *                            threshold), each bank is used as up to 8 slots
+ *                            of the largest RAW container (256-byte aligned),
+ *                            so up to 16 messages are in flight.
  *   h_bank[2]                pinned host banks (cudaHostAlloc / page-locked),
  *                            h_capacity bytes each; message k's container
  *                            lands in h_bank[k % 2] (a later message reuses
