@@ -107,7 +107,10 @@ def test_streams_growing_faster_than_their_exponents_are_read(fmt):
     exponents 64 to 128 times each over a constant run.  The words written
     from the slot's end reach the 1 KiB block of exponent bytes just read
     (all of them) or would pass blocks still to be read (80, 94 and 110 per
-    exponent, which then code from the input); every chunk stays coded."""
+    exponent, which then code from the input); every chunk stays coded.
+    Formats with 4- or 5-bit exponent fields cannot get there: 31 rare
+    symbols add at most ~0.5 KiB of words over their bytes, against the
+    4 KiB the slot keeps above the exponent bytes."""
     bits = synth.growth_bf16() if fmt == "bf16" else synth.growth_fp32()
     comp = _parity(bits)
     c = -(-bits.size // 65536)
