@@ -283,3 +283,51 @@ def test_pipeline_send_ex_keeps_every_container(mode):
             assert np.array_equal(got, want)
             back, status = gu.gpu_decompress(got, gu.BF16, m.size)
             assert status == 0 and np.array_equal(back, m)
+
+
+def _send_all(msgs, mode, raw_below):
+    """uzip_pipeline_send_ex with one host bank per message; returns the
+    containers as numpy arrays."""
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+
+    d_msgs = [gu.to_device(m) for m in msgs]
+    largest = max(m.size for m in msgs)
+    cap = uz.uzip_max_compressed_size(0, largest)
+    banks = [torch.empty(cap, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    hcap = cap + 16 * (-(-largest // 65536))
+    hb = [torch.zeros(hcap, dtype=torch.uint8).pin_memory() for _ in msgs]
+    sizes = torch.zeros(len(msgs), dtype=torch.int64).pin_memory()
+    s0, s1 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    st = uz.uzip_pipeline_send_ex(0, [t.data_ptr() for t in d_msgs], [m.size for m in msgs],
+                                  [b.data_ptr() for b in banks], cap, [h.data_ptr() for h in hb], hcap,
+                                  sizes.data_ptr(), mode, raw_below, s0.cuda_stream, s1.cuda_stream)
+    assert st == 0, uz.uzip_status_string(st)
+    torch.cuda.synchronize()
+    return [hb[k].numpy()[: int(sizes[k])].copy() for k in range(len(msgs))]
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
+def test_pipeline_many_raw_messages_wrap_the_bank_slots(mode):
+    """40 messages under the RAW threshold, 16 to 65,537 values: each device
+    bank is cut into 8 slots, so message k reuses the slot of message k - 16
+    (after its copy); every container equals the oracle's whole-message RAW
+    container (NCCLZ Sec. IV-C)."""
+    msgs = [synth.normal_bf16(16 + ((k * 7919) % 65522), 0.02, 23, k) for k in range(40)]
+    got = _send_all(msgs, mode, 1 << 30)
+    for k, m in enumerate(msgs):
+        want = oracle.compress(m, mode=oracle.MODE_RAW)
+        assert got[k].size == want.size and np.array_equal(got[k], want), f"message {k}"
+
+
+@pytest.mark.parametrize("mode", [0, 3, 4])
+def test_pipeline_mixed_raw_and_coded_messages(mode):
+    """Messages on both sides of an explicit 1 MiB threshold, interleaved:
+    the small ones travel RAW, the large ones coded, through two banks."""
+    msgs = [synth.normal_bf16(((1 << 18) if k % 2 else (1 << 19)) + 31 * k, 0.02, 29, k) for k in range(7)]
+    got = _send_all(msgs, mode, 1 << 20)
+    for k, m in enumerate(msgs):
+        want = oracle.compress(m, mode=oracle.MODE_RAW if 2 * m.size < (1 << 20) else oracle.MODE_CHUNK)
+        assert got[k].size == want.size and np.array_equal(got[k], want), f"message {k}"
