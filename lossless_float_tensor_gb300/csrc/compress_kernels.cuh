@@ -1247,14 +1247,14 @@ __global__ void __launch_bounds__(32) raw_kernel(CompressArgs a) {
 // launcher of one format and mode (instantiated in compress_fmt_*.cu)
 
 // the warp-specialised compressor (compress_ws.cuh)
-template <int DT>
+template <int DT, bool SAMPLED>
 cudaError_t launch_ws(const CompressArgs& a, cudaStream_t s);
 
 // Launches the kernels of one compression mode (0: per-chunk choice, 1: whole
 // message RAW, 2: gated, 3: sampled tables) for element format DT.  With a
-// slot area, modes 0 and 2 code with the warp-specialised compressor; the
-// sampled tables, and every mode without a slot area (the allocation-free
-// entry point), use the one-warp compressor.
+// slot area, modes 0, 2 and 3 code with the warp-specialised compressor;
+// without one (the allocation-free entry point) the one-warp compressor
+// codes.
 template <int DT>
 cudaError_t launch_mode(CompressArgs a, int mode, bool stash, cudaStream_t s) {
     cudaError_t err;
@@ -1276,7 +1276,8 @@ cudaError_t launch_mode(CompressArgs a, int mode, bool stash, cudaStream_t s) {
         raw_kernel<DT><<<dim3(uint32_t(grid)), dim3(32), 0, s>>>(a);
         if ((err = cudaGetLastError()) != cudaSuccess || mode == 1) return err;
     }
-    if ((mode == 0 || mode == 2) && stash && C > 0) return launch_ws<DT>(a, s);
+    if ((mode == 0 || mode == 2) && stash && C > 0) return launch_ws<DT, false>(a, s);
+    if (mode == 3 && stash && C > 0) return launch_ws<DT, true>(a, s);
     void (*kern)(CompressArgs) = mode == 3 ? compress_kernel<DT, true> : compress_kernel<DT, false>;
     if ((err = launch_shape(reinterpret_cast<const void*>(kern), 32, kCompressSmem, &sms, &per_sm)) != cudaSuccess)
         return err;

@@ -109,8 +109,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 // The pass over one chunk for formats with whole-byte fields.  A unit is 16
 // consecutive values of one lane: its remainder bytes and its 16 exponent
 // bytes leave as 16-byte stores; every exponent increments row e, column
-// lane mod 16 of the histogram (red.shared).
-template <int DT>
+// lane mod 16 of the histogram (red.shared).  CM 2 (sampled tables): only the
+// exponents at positions 0, 16, 32, ... of the chunk are counted, i.e. each
+// unit's first.
+template <int DT, int CM = 1>
 __device__ void ws_split_bytes(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* __restrict__ rem_dst,
                                uint8_t* __restrict__ ex_dst, uint32_t hist_s, uint32_t lane, uint64_t pol) {
     constexpr uint32_t es = Fmt<DT>::kEs;
@@ -130,10 +132,12 @@ __device__ void ws_split_bytes(const uint8_t* __restrict__ cin, uint32_t n_c, ui
                 const uint32_t sg = prmt(a, b, 0xFDB9);  // high bytes, sign replicated
                 r[g] = (lo & 0x7F7F7F7Fu) | (sg & 0x80808080u);
                 ex[g] = prmt(a << 1, b << 1, 0x7531);
-                red_shared_inc(hist_s + (((a >> 1) & 0x3FC0u) | lane4));
-                red_shared_inc(hist_s + (((a >> 17) & 0x3FC0u) | lane4));
-                red_shared_inc(hist_s + (((b >> 1) & 0x3FC0u) | lane4));
-                red_shared_inc(hist_s + (((b >> 17) & 0x3FC0u) | lane4));
+                if (CM == 1 || g == 0) red_shared_inc(hist_s + (((a >> 1) & 0x3FC0u) | lane4));
+                if (CM == 1) {
+                    red_shared_inc(hist_s + (((a >> 17) & 0x3FC0u) | lane4));
+                    red_shared_inc(hist_s + (((b >> 1) & 0x3FC0u) | lane4));
+                    red_shared_inc(hist_s + (((b >> 17) & 0x3FC0u) | lane4));
+                }
             }
             st_v4_hint(rem_dst + uint64_t(unit) * 16, make_uint4(r[0], r[1], r[2], r[3]), pol);
         } else {
@@ -151,10 +155,12 @@ __device__ void ws_split_bytes(const uint8_t* __restrict__ cin, uint32_t n_c, ui
                 r[3 * g] = prmt(prmt(a, t, 0x0410), b, 0x4210);      // a0 a1 t0 b0
                 r[3 * g + 1] = prmt(prmt(b, t, 0x0051), c, 0x5410);  // b1 t1 c0 c1
                 r[3 * g + 2] = prmt(d, t, 0x7106);                   // t2 d0 d1 t3
-                red_shared_inc(hist_s + (((a >> 17) & 0x3FC0u) | lane4));
-                red_shared_inc(hist_s + (((b >> 17) & 0x3FC0u) | lane4));
-                red_shared_inc(hist_s + (((c >> 17) & 0x3FC0u) | lane4));
-                red_shared_inc(hist_s + (((d >> 17) & 0x3FC0u) | lane4));
+                if (CM == 1 || g == 0) red_shared_inc(hist_s + (((a >> 17) & 0x3FC0u) | lane4));
+                if (CM == 1) {
+                    red_shared_inc(hist_s + (((b >> 17) & 0x3FC0u) | lane4));
+                    red_shared_inc(hist_s + (((c >> 17) & 0x3FC0u) | lane4));
+                    red_shared_inc(hist_s + (((d >> 17) & 0x3FC0u) | lane4));
+                }
             }
             uint8_t* dr = rem_dst + uint64_t(unit) * 48;
 #pragma unroll
@@ -199,7 +205,7 @@ __device__ void ws_split_bytes(const uint8_t* __restrict__ cin, uint32_t n_c, ui
         const uint32_t e = Traits<DT>::exp_of(b);
 #pragma unroll
         for (uint32_t k = 0; k < es - 1; ++k) rem_dst[(es - 1) * uint64_t(i) + k] = uint8_t(r >> (8 * k));
-        red_shared_inc(hist_s + ((e << 6) | lane4));
+        if (CM == 1 || (i & 15u) == 0) red_shared_inc(hist_s + ((e << 6) | lane4));
         ex_dst[i] = uint8_t(e);
     }
 }
@@ -207,7 +213,8 @@ __device__ void ws_split_bytes(const uint8_t* __restrict__ cin, uint32_t n_c, ui
 // The same pass for formats whose sign|fraction field is not a whole number
 // of bytes (fp16: 11 bits, fp8 e4m3fn: 4, e5m2: 3): a unit is 32 values, whose
 // W-bit fields pack into exactly W 32-bit words, least significant bit first.
-template <int DT>
+// CM 2: only the unit's values 0 and 16 are counted.
+template <int DT, int CM = 1>
 __device__ void ws_split_packed(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* __restrict__ rem_dst,
                                 uint8_t* __restrict__ ex_dst, uint32_t hist_s, uint32_t lane, uint64_t pol) {
     constexpr uint32_t es = Fmt<DT>::kEs, mb = Fmt<DT>::kMbits, W = Fmt<DT>::kRbits;
@@ -226,8 +233,8 @@ __device__ void ws_split_packed(const uint8_t* __restrict__ cin, uint32_t n_c, u
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const uint32_t eb = (w[j] >> mb) & em2;  // both exponents, bytes 0 and 2
-                count((eb << 6) & 0x3FC0u);
-                count((eb >> 10) & 0x3FC0u);
+                if (CM == 1 || j == 0 || j == 8) count((eb << 6) & 0x3FC0u);
+                if (CM == 1) count((eb >> 10) & 0x3FC0u);
                 f[2 * j] = Traits<DT>::rem_of(w[j] & 0xFFFFu);
                 f[2 * j + 1] = Traits<DT>::rem_of(w[j] >> 16);
                 if (j & 1) ex[j >> 1] = __byte_perm((w[j - 1] >> mb) & em2, eb, 0x6420);
@@ -237,10 +244,12 @@ __device__ void ws_split_packed(const uint8_t* __restrict__ cin, uint32_t n_c, u
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 ex[j] = (w[j] >> mb) & em4;
-                count((ex[j] << 6) & 0x3FC0u);
-                count((ex[j] >> 2) & 0x3FC0u);
-                count((ex[j] >> 10) & 0x3FC0u);
-                count((ex[j] >> 18) & 0x3FC0u);
+                if (CM == 1 || j == 0 || j == 4) count((ex[j] << 6) & 0x3FC0u);
+                if (CM == 1) {
+                    count((ex[j] >> 2) & 0x3FC0u);
+                    count((ex[j] >> 10) & 0x3FC0u);
+                    count((ex[j] >> 18) & 0x3FC0u);
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) f[4 * j + k] = Traits<DT>::rem_of((w[j] >> (8 * k)) & 0xFFu);
             }
@@ -307,7 +316,7 @@ __device__ void ws_split_packed(const uint8_t* __restrict__ cin, uint32_t n_c, u
         }
         for (uint32_t i = i0 + lane; i < n_c; i += 32) {
             const uint32_t e = Traits<DT>::exp_of(Traits<DT>::load(cin, i));
-            count(e << 6);
+            if (CM == 1 || (i & 15u) == 0) count(e << 6);
             ex_dst[i] = uint8_t(e);
         }
     }
@@ -453,7 +462,7 @@ __device__ void ws_place(const CompressArgs& a, uint8_t* meta, uint8_t* ctx, uin
 // encoders' contexts in order, place the chunk the context held, wait until
 // the encoder is far enough into its other context, take the next chunk,
 // split it into the context and mark it ready.
-template <int DT>
+template <int DT, bool SAMPLED>
 __device__ void ws_helper(const CompressArgs& a, uint8_t* smem, uint32_t h, uint32_t lane) {
     const uint32_t C = a.num_chunks;
     const uint32_t processed = C - a.first_ticket;
@@ -519,14 +528,27 @@ __device__ void ws_helper(const CompressArgs& a, uint8_t* smem, uint32_t h, uint
         }
         __syncwarp();
         uint8_t* rem_dst = a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk;
-        if constexpr (Fmt<DT>::kPacked) ws_split_packed<DT>(cin, n_c, rem_dst, ctx, hist_s, lane, pol);
-        else ws_split_bytes<DT>(cin, n_c, rem_dst, ctx, hist_s, lane, pol);
+        if constexpr (Fmt<DT>::kPacked) ws_split_packed<DT, SAMPLED ? 2 : 1>(cin, n_c, rem_dst, ctx, hist_s, lane, pol);
+        else ws_split_bytes<DT, SAMPLED ? 2 : 1>(cin, n_c, rem_dst, ctx, hist_s, lane, pol);
         __syncwarp();
         if (a.progress) post_progress(a.progress + 2 * uint64_t(c), 1, lane);
         uint32_t cnt[8];
         reduce_hist(hsm, lane, cnt);
         Norm nm;
-        normalise(cnt, n_c, lane, regB, nm);
+        uint32_t total = n_c;  // the counts' total
+        if constexpr (SAMPLED) {  // a seen symbol counts 16 x, an unseen one of the format's range 1
+            uint32_t part = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t sym = 8 * lane + k;
+                cnt[k] = cnt[k] ? 16 * cnt[k] : (sym < (1u << Fmt<DT>::kEbits) ? 1u : 0u);
+                part += cnt[k];
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
+            total = part;
+        }
+        normalise<SAMPLED>(cnt, total, lane, regB, nm);
         ws_build_table(nm, lane, table_s, meta);
         if (lane == 0) {
             *reinterpret_cast<volatile uint32_t*>(meta + kMetaChunk) = c;
@@ -797,7 +819,7 @@ __device__ void ws_encoder(const CompressArgs& a, uint8_t* smem, uint32_t e, uin
     }
 }
 
-template <int DT>
+template <int DT, bool SAMPLED>
 __global__ void __launch_bounds__(kWsThreads, 1) compress_ws_kernel(CompressArgs a) {
     extern __shared__ __align__(128) uint8_t ws_smem[];
     uint8_t* smem = ws_smem;
@@ -812,12 +834,12 @@ __global__ void __launch_bounds__(kWsThreads, 1) compress_ws_kernel(CompressArgs
     }
     __syncthreads();
     if (warp < kWsEnc) ws_encoder<DT>(a, smem, warp, lane);
-    else ws_helper<DT>(a, smem, warp - kWsEnc, lane);
+    else ws_helper<DT, SAMPLED>(a, smem, warp - kWsEnc, lane);
 }
 
-template <int DT>
+template <int DT, bool SAMPLED>
 cudaError_t launch_ws(const CompressArgs& a, cudaStream_t s) {
-    void (*kern)(CompressArgs) = compress_ws_kernel<DT>;
+    void (*kern)(CompressArgs) = compress_ws_kernel<DT, SAMPLED>;
     cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, int(kWsSmem));
     if (err != cudaSuccess) return err;
