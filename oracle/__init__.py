@@ -38,7 +38,8 @@ def build(force: bool = False) -> str:
     )
     if stale:
         tmp = LIB_PATH + ".tmp.%d" % os.getpid()
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-Wall", "-Wextra", "-shared", "-fPIC", "-o", tmp] + SOURCES)
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-Wall", "-Wextra", "-shared", "-fPIC", "-o", tmp] + SOURCES
+                              + ["-lm"])
         os.replace(tmp, LIB_PATH)
     return LIB_PATH
 
@@ -77,6 +78,11 @@ def lib():
         L.orc_gate_says_raw.restype = ctypes.c_int
         L.orc_sampled_counts.argtypes = [vp, ctypes.c_uint32, ctypes.c_int, vp]
         L.orc_sampled_counts.restype = ctypes.c_uint32
+        L.orc_parametric_counts.argtypes = [ctypes.c_int, ctypes.c_double, vp]
+        L.orc_parametric_counts.restype = ctypes.c_uint32
+        L.orc_compress_parametric.argtypes = [ctypes.c_int, vp, ctypes.c_uint64, vp, ctypes.c_uint64, u64p,
+                                              ctypes.c_double]
+        L.orc_compress_parametric.restype = ctypes.c_int
         L.orc_compress.argtypes = [ctypes.c_int, vp, ctypes.c_uint64, vp, ctypes.c_uint64, u64p]
         L.orc_decompress.argtypes = [vp, ctypes.c_uint64, ctypes.c_int, ctypes.c_uint64, vp]
         for name in ("orc_split", "orc_merge", "orc_normalise", "orc_rans_encode", "orc_rans_decode",
@@ -205,22 +211,36 @@ def container_bound(dtype: int, n: int) -> int:
     return int(lib().orc_container_bound(dtype, n))
 
 
-MODE_CHUNK, MODE_RAW, MODE_GATE, MODE_SAMPLED = 0, 1, 2, 3
+MODE_CHUNK, MODE_RAW, MODE_GATE, MODE_SAMPLED, MODE_PARAMETRIC = 0, 1, 2, 3, 4
 
 
-def compress(bits: np.ndarray, dtype: int | None = None, mode: int = MODE_CHUNK) -> np.ndarray:
+def compress(bits: np.ndarray, dtype: int | None = None, mode: int = MODE_CHUNK,
+             sigma: float | None = None) -> np.ndarray:
     """Container bytes for an array of element bit patterns (see dtype_code;
     fp8 needs dtype=FP8_E4M3 or FP8_E5M2 with uint8 bits).  mode: per-chunk
-    choice, whole-message RAW, RAW when the gate's sample says so, or tables
-    built from a sample of each chunk."""
+    choice, whole-message RAW, RAW when the gate's sample says so, tables
+    built from a sample of each chunk, or (MODE_PARAMETRIC, with sigma) the
+    one Gaussian-model table of R25 for every chunk."""
     d, bits = _bits(bits, dtype)
     n = bits.size
     cap = container_bound(d, n)
     out = np.empty(max(cap, 1), np.uint8)
     total = ctypes.c_uint64(0)
     src = bits if n else np.zeros(1, bits.dtype)
-    _check(lib().orc_compress_mode(d, _ptr(src), n, _ptr(out), cap, ctypes.byref(total), mode), "compress")
+    if mode == MODE_PARAMETRIC:
+        st = lib().orc_compress_parametric(d, _ptr(src), n, _ptr(out), cap, ctypes.byref(total), float(sigma))
+    else:
+        st = lib().orc_compress_mode(d, _ptr(src), n, _ptr(out), cap, ctypes.byref(total), mode)
+    _check(st, "compress")
     return out[: total.value].copy()
+
+
+def parametric_counts(dtype: int, sigma: float):
+    """R25 model counts for values ~ N(0, sigma^2) and their total (0 for a
+    sigma that is not finite and positive)."""
+    counts = np.zeros(256, np.uint32)
+    total = lib().orc_parametric_counts(dtype, float(sigma), _ptr(counts))
+    return counts, int(total)
 
 
 def gate_says_raw(bits: np.ndarray, dtype: int | None = None) -> bool:

@@ -12,6 +12,9 @@
  *                          fraction); R1 byte layout of the remainder.
  *   local tables ......... UCCL-Zip Fig. 5 caption (each block builds its own
  *                          table); R3 chunking, R4 histogram, R5 normalisation.
+ *   parametric tables .... ZipCCL abstract (exponent coding from the
+ *                          Gaussian shape of the values, without online
+ *                          statistics); R25 model counts.
  *   entropy coder ........ UCCL-Zip Fig. 2 caption ("ANS"); R6 rANS constants,
  *                          R7 lane interleaving and word order, R8 stream.
  *   RAW fallback ......... NCCLZ Sec. IV-B and IV-C, Alg. 1 (store RAW when
@@ -22,6 +25,7 @@
  */
 #include "uzip_oracle.h"
 
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -339,6 +343,34 @@ uint32_t orc_sampled_counts(const uint8_t* exps, uint32_t n_c, int ebits, uint32
     return total;
 }
 
+/* R25: counts of the parametric table for values ~ N(0, sigma^2) (ZipCCL
+ * abstract: the exponent coding follows from the Gaussian shape, with no
+ * statistics gathered online).  With bias b = 2^(ebits-1) - 1, exponent field
+ * e >= 1 holds the magnitudes [2^(e-b), 2^(e-b+1)), whose probability is
+ * erfc(x_e) - erfc(2 x_e) for x_e = 2^(e-b) / (sigma sqrt 2); e = 0 holds
+ * zero and the subnormals, |x| < 2^(1-b): probability 1 - erfc(2 x_0).  Each
+ * probability becomes a count out of 65536, rounded to nearest, and every
+ * symbol of [0, 2^ebits) counts at least 1 so that any value stays codable.
+ * Returns the counts' total, or 0 for an unknown dtype or a sigma that is
+ * not finite and positive. */
+uint32_t orc_parametric_counts(int dtype, double sigma, uint32_t counts[256]) {
+    int ebits, mbits, es;
+    for (int s = 0; s < 256; ++s) counts[s] = 0;
+    if (!layout(dtype, &ebits, &mbits, &es) || !(sigma > 0.0) || !isfinite(sigma)) return 0;
+    const int bias = (1 << (ebits - 1)) - 1;
+    const double scale = sigma * sqrt(2.0);
+    uint32_t total = 0;
+    for (int e = 0; e < (1 << ebits); ++e) {
+        const double x = ldexp(1.0, e - bias) / scale;
+        const double p = e == 0 ? 1.0 - erfc(2.0 * x) : erfc(x) - erfc(2.0 * x);
+        double c = floor(65536.0 * p + 0.5);
+        if (c < 1.0) c = 1.0;
+        counts[e] = (uint32_t)c;
+        total += counts[e];
+    }
+    return total;
+}
+
 int orc_encode_chunk_freq(const uint8_t* exps, uint32_t n_c, const uint16_t freq[256], int force_coded,
                           uint8_t* out, uint32_t* len, int* raw) {
     if (n_c == 0 || n_c > ORC_CHUNK_ELEMS) return ORC_ERR_INVALID_ARG;
@@ -482,10 +514,10 @@ int orc_compress(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t c
     return orc_compress_mode(dtype, in, n, out, cap, total, ORC_MODE_CHUNK);
 }
 
-int orc_compress_mode(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t cap,
-                      uint64_t* total, int mode) {
-    if (mode != ORC_MODE_CHUNK && mode != ORC_MODE_RAW && mode != ORC_MODE_GATE && mode != ORC_MODE_SAMPLED)
-        return ORC_ERR_INVALID_ARG;
+/* The container of every mode; model (R25) is the one table of every chunk,
+ * or NULL. */
+static int compress_impl(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t cap, uint64_t* total,
+                         int mode, const uint16_t* model) {
     if (!dtype_ok(dtype)) return ORC_ERR_UNSUPPORTED_DTYPE;
     if (num_chunks(n) > 0xFFFFFFFFull) return ORC_ERR_INVALID_ARG;
     if ((n > 0 && in == NULL) || out == NULL) return ORC_ERR_INVALID_ARG;
@@ -519,6 +551,8 @@ int orc_compress_mode(int dtype, const void* in, uint64_t n, uint8_t* out, uint6
             memcpy(out + exp_offset + off, exps + c * ORC_CHUNK_ELEMS, n_c);
             len = n_c;
             raw = 1;
+        } else if (model != NULL) {
+            st = orc_encode_chunk_freq(exps + c * ORC_CHUNK_ELEMS, n_c, model, 0, out + exp_offset + off, &len, &raw);
         } else if (mode == ORC_MODE_SAMPLED) {
             int ebits, mbits, es;
             layout(dtype, &ebits, &mbits, &es);
@@ -557,6 +591,27 @@ int orc_compress_mode(int dtype, const void* in, uint64_t n, uint8_t* out, uint6
     wr_le(h + 40, exp_offset + off, 8);
     *total = exp_offset + off;
     return ORC_OK;
+}
+
+int orc_compress_mode(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t cap,
+                      uint64_t* total, int mode) {
+    if (mode != ORC_MODE_CHUNK && mode != ORC_MODE_RAW && mode != ORC_MODE_GATE && mode != ORC_MODE_SAMPLED)
+        return ORC_ERR_INVALID_ARG;
+    return compress_impl(dtype, in, n, out, cap, total, mode, NULL);
+}
+
+/* R25: every chunk coded (or stored RAW, R9) with the one table R5 makes of
+ * orc_parametric_counts(dtype, sigma). */
+int orc_compress_parametric(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t cap,
+                            uint64_t* total, double sigma) {
+    if (!dtype_ok(dtype)) return ORC_ERR_UNSUPPORTED_DTYPE;
+    uint32_t counts[256];
+    uint16_t freq[256];
+    const uint32_t sum = orc_parametric_counts(dtype, sigma, counts);
+    if (sum == 0) return ORC_ERR_INVALID_ARG;
+    const int st = orc_normalise(counts, sum, freq);
+    if (st != ORC_OK) return st;
+    return compress_impl(dtype, in, n, out, cap, total, ORC_MODE_CHUNK, freq);
 }
 
 /* R12: the receiver checks the header and every chunk before trusting it. */

@@ -119,6 +119,15 @@ int orc_compress_mode(int dtype, const void* in, uint64_t n, uint8_t* out, uint6
  * symbol counts 16 x its sample count, an unseen one of [0, 2^ebits) counts
  * 1); returns their total. */
 uint32_t orc_sampled_counts(const uint8_t* exps, uint32_t n_c, int ebits, uint32_t counts[256]);
+/* R25 parametric-table counts for values ~ N(0, sigma^2): for each exponent
+ * field value of the format, the probability of its binade as a count out of
+ * 65536 (rounded to nearest, at least 1); returns their total, 0 for an
+ * unknown dtype or a sigma that is not finite and positive. */
+uint32_t orc_parametric_counts(int dtype, double sigma, uint32_t counts[256]);
+/* R25: every chunk coded with the one table normalised (R5) from
+ * orc_parametric_counts, or stored RAW where that is not shorter (R9). */
+int orc_compress_parametric(int dtype, const void* in, uint64_t n, uint8_t* out, uint64_t cap,
+                            uint64_t* total, double sigma);
 /* One chunk stream coded with the given table (every symbol of exps must have
  * freq > 0); RAW unless shorter, as orc_encode_chunk. */
 int orc_encode_chunk_freq(const uint8_t* exps, uint32_t n_c, const uint16_t freq[256], int force_coded,
