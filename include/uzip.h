@@ -191,6 +191,28 @@ uzip_status uzip_compress_noalloc(const void* d_in, uzip_dtype dtype, uint64_t n
 uzip_status uzip_decompress(const void* d_comp, uint64_t comp_capacity, void* d_out,
                             uzip_dtype dtype, uint64_t n, int32_t* d_status, cudaStream_t s);
 
+/* Compression with one Gaussian-model table for every chunk (ZipCCL abstract:
+ * exponent coding that follows from the Gaussian shape of LLM tensors, with
+ * no statistics gathered online), for values ~ N(0, sigma^2):
+ *   sigma         finite and > 0 (else UZIP_ERR_INVALID_ARG, nothing
+ *                 enqueued), e.g. a weight initialisation's standard
+ *                 deviation.  For exponent field e >= 1 of a format with bias
+ *                 b the model's probability is erfc(x) - erfc(2x), x =
+ *                 2^(e-b) / (sigma sqrt 2) (the binade [2^(e-b), 2^(e-b+1))
+ *                 on both sides of zero), for e = 0 it is 1 - erfc(2x); each
+ *                 becomes a count out of 65536 (rounded to nearest, at least
+ *                 1 for every value of the field) and the counts are
+ *                 normalised to 4096 like a chunk's histogram.
+ * The helper warps then count nothing: every chunk is coded with that one
+ * table, or stored RAW where coding does not shrink it.  Every value stays
+ * codable whatever sigma is; a sigma far from the data's only costs size.
+ * The container format is unchanged (each coded chunk lists all 2^ebits
+ * symbols), so uzip_decompress reads it.  Other arguments and errors as for
+ * uzip_compress_ex. */
+uzip_status uzip_compress_parametric(const void* d_in, uzip_dtype dtype, uint64_t n, void* d_out,
+                                     uint64_t out_capacity, uint64_t* d_out_size, int32_t* d_status, double sigma,
+                                     cudaStream_t s);
+
 /* Compression with a whole-message choice (NCCLZ Sec. IV-C and Alg. 1: a
  * message whose coding would not pay travels RAW; it samples at most 64 KiB).
  * The container format is the one above; only the choice differs:

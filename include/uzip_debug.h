@@ -25,6 +25,12 @@ int uzip_debug_div_magic(uint32_t f, uint32_t* m, uint32_t* add, uint32_t* shift
  * constants for a valid f, 0 for f outside [1, 4096]. */
 int uzip_debug_div_magic33(uint32_t f, uint32_t* m_lo, uint32_t* shift);
 
+/* The counts uzip_compress_parametric normalises into its table, for values
+ * ~ N(0, sigma^2) of format dtype (counts[256]; values beyond the format's
+ * exponent field are 0).  Returns 1, or 0 for an unknown dtype or a sigma
+ * that is not finite and positive. */
+int uzip_debug_model_counts(int dtype, double sigma, uint32_t* counts);
+
 /* Tuning of the warp-specialised compressor: a helper warp starts splitting
  * its encoder's next chunk once the encoder has at most `blocks` blocks of 32
  * steps left of its current chunk (64: at once).  Default 32.  Affects speed

@@ -48,6 +48,8 @@ _lib.uzip_compress_ex.argtypes = [_vp, _int, _u64, _vp, _u64, _vp, _vp, _u32, _v
 _lib.uzip_compress_ex.restype = _int
 _lib.uzip_compress_noalloc.argtypes = [_vp, _int, _u64, _vp, _u64, _vp, _vp, _vp]
 _lib.uzip_compress_noalloc.restype = _int
+_lib.uzip_compress_parametric.argtypes = [_vp, _int, _u64, _vp, _u64, _vp, _vp, ctypes.c_double, _vp]
+_lib.uzip_compress_parametric.restype = _int
 _lib.uzip_compress_gated.argtypes = [_vp, _int, _u64, _vp, _u64, _vp, _vp, _u64, _vp]
 _lib.uzip_compress_gated.restype = _int
 _lib.uzip_decompress.argtypes = [_vp, _u64, _vp, _int, _u64, _vp, _vp]
@@ -64,6 +66,8 @@ _lib.uzip_pipeline_send_ex.argtypes = [_int, ctypes.POINTER(_vp), ctypes.POINTER
 _lib.uzip_pipeline_send_ex.restype = _int
 _lib.uzip_debug_div_magic.argtypes = [_u32, ctypes.POINTER(_u32), ctypes.POINTER(_u32), ctypes.POINTER(_u32)]
 _lib.uzip_debug_div_magic.restype = _int
+_lib.uzip_debug_model_counts.argtypes = [_int, ctypes.c_double, ctypes.POINTER(_u32)]
+_lib.uzip_debug_model_counts.restype = _int
 _lib.uzip_debug_scratch_offset.argtypes = [_int, _u64]
 _lib.uzip_debug_scratch_offset.restype = _u64
 
@@ -93,6 +97,14 @@ def uzip_compress_gated(d_in: int, dtype: int, n: int, d_out: int, out_capacity:
                         d_status: int | None, raw_below_bytes: int, stream: int) -> int:
     return int(_lib.uzip_compress_gated(d_in, dtype, n, d_out, out_capacity, d_out_size, d_status, raw_below_bytes,
                                         stream))
+
+
+def uzip_compress_parametric(d_in: int, dtype: int, n: int, d_out: int, out_capacity: int, d_out_size: int | None,
+                             d_status: int | None, sigma: float, stream: int) -> int:
+    """Compression with one Gaussian-model table for every chunk (values ~
+    N(0, sigma^2)); see include/uzip.h."""
+    return int(_lib.uzip_compress_parametric(d_in, dtype, n, d_out, out_capacity, d_out_size, d_status, float(sigma),
+                                             stream))
 
 
 def uzip_compress_noalloc(d_in: int, dtype: int, n: int, d_out: int, out_capacity: int, d_out_size: int | None,

@@ -128,6 +128,29 @@ uzip_status uzip_compress(const void* d_in, uzip_dtype dtype, uint64_t n, void* 
     return uzip_compress_ex(d_in, dtype, n, d_out, out_capacity, d_out_size, nullptr, 0, s);
 }
 
+uzip_status uzip_compress_parametric(const void* d_in, uzip_dtype dtype, uint64_t n, void* d_out,
+                                     uint64_t out_capacity, uint64_t* d_out_size, int32_t* d_status, double sigma,
+                                     cudaStream_t s) {
+    if (!valid_dtype(dtype)) return UZIP_ERR_UNSUPPORTED_DTYPE;
+    if (n > UZIP_MAX_ELEMS) return UZIP_ERR_INVALID_ARG;
+    if (n > 0 && (d_in == nullptr || !aligned(d_in, 16))) return UZIP_ERR_INVALID_ARG;
+    if (d_out == nullptr || !aligned(d_out, 16)) return UZIP_ERR_INVALID_ARG;
+    if (d_out_size && !aligned(d_out_size, 8)) return UZIP_ERR_INVALID_ARG;
+    if (d_status && !aligned(d_status, 4)) return UZIP_ERR_INVALID_ARG;
+    uint32_t model[256];
+    if (!model_counts(dtype, sigma, model)) return UZIP_ERR_INVALID_ARG;
+    const uint64_t need = uzip_max_compressed_size(dtype, n);
+    if (out_capacity < need) return UZIP_ERR_CAPACITY;
+    if (!device_range_ok(d_in, n * elem_bytes(dtype)) || !device_range_ok(d_out, need) ||
+        (d_out_size && !device_range_ok(d_out_size, 8)) || (d_status && !device_range_ok(d_status, 4)))
+        return UZIP_ERR_INVALID_ARG;
+    if (launch_compress(dtype, d_in, n, d_out, d_out_size, d_status, 0, s, 4, nullptr, model) != cudaSuccess) {
+        cudaGetLastError();
+        return UZIP_ERR_CUDA;
+    }
+    return UZIP_OK;
+}
+
 uzip_status uzip_compress_gated(const void* d_in, uzip_dtype dtype, uint64_t n, void* d_out, uint64_t out_capacity,
                                 uint64_t* d_out_size, int32_t* d_status, uint64_t raw_below_bytes, cudaStream_t s) {
     if (!valid_dtype(dtype)) return UZIP_ERR_UNSUPPORTED_DTYPE;
@@ -253,6 +276,11 @@ int uzip_debug_div_magic33(uint32_t f, uint32_t* m_lo, uint32_t* shift) {
 }
 
 void uzip_debug_set_ws_jit_blocks(uint32_t blocks) { g_ws_jit_blocks = blocks; }
+
+int uzip_debug_model_counts(int dtype, double sigma, uint32_t* counts) {
+    if (!counts || !valid_dtype(dtype)) return 0;
+    return model_counts(dtype, sigma, counts) ? 1 : 0;
+}
 
 uint64_t uzip_debug_scratch_offset(uzip_dtype dtype, uint64_t n) {
     if (!valid_dtype(dtype) || n > UZIP_MAX_ELEMS) return 0;

@@ -3,6 +3,8 @@
 // and is compiled once per element format (compress_fmt_*.cu).
 #include <cuda.h>
 
+#include <cmath>
+
 #include <mutex>
 
 #include "compress_kernels.cuh"
@@ -27,7 +29,7 @@ extern template cudaError_t launch_mode<UZIP_FP8_E5M2>(CompressArgs, int, bool, 
 // the container's bytes of d_out are written).
 cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                                          int32_t* d_status, uint32_t first_ticket, void* scratch_area, void* stash,
-                                         cudaStream_t s, int mode, uint64_t* progress) {
+                                         cudaStream_t s, int mode, uint64_t* progress, const uint32_t* model) {
     const uint64_t C = num_chunks(n);
     uint8_t* out = static_cast<uint8_t*>(d_out);
     Scratch* scratch = static_cast<Scratch*>(scratch_area);
@@ -49,6 +51,11 @@ cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n
     a.gated = 0;
     a.progress = progress;
     a.jit_blocks = g_ws_jit_blocks;
+    a.model_total = 0;
+    for (int e = 0; e < 256; ++e) {
+        a.model[e] = model ? model[e] : 0u;
+        a.model_total += a.model[e];
+    }
     const bool has_stash = stash != nullptr;
     switch (dtype) {
         case UZIP_BF16: return launch_mode<UZIP_BF16>(a, mode, has_stash, s);
@@ -62,11 +69,46 @@ cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n
 // The regular path: the work area (counters, descriptors, slots) sits in the
 // caller's output buffer, behind the largest possible container.
 cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
-                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s, int mode, uint64_t* progress) {
+                            int32_t* d_status, uint32_t first_ticket, cudaStream_t s, int mode, uint64_t* progress,
+                            const uint32_t* model) {
     uint8_t* work = static_cast<uint8_t*>(d_out) + scratch_offset(dtype, n);
     const uintptr_t st = (reinterpret_cast<uintptr_t>(work) + scratch_bytes(n) + 4095) & ~uintptr_t(4095);
     return launch_compress_with_scratch(dtype, d_in, n, d_out, d_out_size, d_status, first_ticket, work,
-                                        reinterpret_cast<void*>(st), s, mode, progress);
+                                        reinterpret_cast<void*>(st), s, mode, progress, model);
+}
+
+// Counts of the Gaussian-model table (ZipCCL abstract: the exponent coding
+// follows from the values' Gaussian shape, no statistics gathered online)
+// for values ~ N(0, sigma^2).  Exponent field e of a format with bias b holds
+// the magnitudes [2^(e-b), 2^(e-b+1)) (e >= 1) or [0, 2^(1-b)) (e = 0); with
+// the normal distribution's tail erfc(t / sqrt 2), the binade's probability
+// is erfc(x) - erfc(2x) for x = 2^(e-b) / (sigma sqrt 2), and 1 - erfc(2x)
+// for e = 0.  Each probability becomes a count out of 65536 rounded to
+// nearest, and every value of the field counts at least 1, so that any
+// tensor stays codable.  Returns false for a sigma that is not finite and
+// positive.
+bool model_counts(int dtype, double sigma, uint32_t counts[256]) {
+    for (int e = 0; e < 256; ++e) counts[e] = 0;
+    if (!(sigma > 0.0) || !std::isfinite(sigma)) return false;
+    int ebits = 0;
+    switch (dtype) {
+        case UZIP_BF16: ebits = Fmt<UZIP_BF16>::kEbits; break;
+        case UZIP_FP32: ebits = Fmt<UZIP_FP32>::kEbits; break;
+        case UZIP_FP16: ebits = Fmt<UZIP_FP16>::kEbits; break;
+        case UZIP_FP8_E4M3: ebits = Fmt<UZIP_FP8_E4M3>::kEbits; break;
+        case UZIP_FP8_E5M2: ebits = Fmt<UZIP_FP8_E5M2>::kEbits; break;
+        default: return false;
+    }
+    const int b = (1 << (ebits - 1)) - 1;
+    const double unit = sigma * std::sqrt(2.0);  // sigma sqrt 2
+    for (int e = 0; e < (1 << ebits); ++e) {
+        const double x = std::ldexp(1.0, e - b) / unit;
+        const double tail_lo = std::erfc(x), tail_hi = std::erfc(2.0 * x);
+        const double p = e == 0 ? 1.0 - tail_hi : tail_lo - tail_hi;
+        const double c = std::floor(65536.0 * p + 0.5);
+        counts[e] = c < 1.0 ? 1u : uint32_t(c);
+    }
+    return true;
 }
 
 // ---------------------------------------------------------------------------

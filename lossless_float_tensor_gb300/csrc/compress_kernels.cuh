@@ -47,6 +47,10 @@ struct CompressArgs {
     // once its encoder has at most this many blocks of 32 steps left of the
     // current one (64 or more: at once)
     uint32_t jit_blocks;
+    // mode 4 (parametric tables): the model counts of every exponent field
+    // value and their total, the same for every chunk
+    uint32_t model_total;
+    uint32_t model[256];
 };
 
 // element traits --------------------------------------------------------------
@@ -1247,14 +1251,16 @@ __global__ void __launch_bounds__(32) raw_kernel(CompressArgs a) {
 // launcher of one format and mode (instantiated in compress_fmt_*.cu)
 
 // the warp-specialised compressor (compress_ws.cuh)
-template <int DT, bool SAMPLED>
+// TM, the table of each chunk: 0 its histogram, 1 a sample of it, 2 the
+// caller's Gaussian model
+template <int DT, int TM>
 cudaError_t launch_ws(const CompressArgs& a, cudaStream_t s);
 
 // Launches the kernels of one compression mode (0: per-chunk choice, 1: whole
-// message RAW, 2: gated, 3: sampled tables) for element format DT.  With a
-// slot area, modes 0, 2 and 3 code with the warp-specialised compressor;
-// without one (the allocation-free entry point) the one-warp compressor
-// codes.
+// message RAW, 2: gated, 3: sampled tables, 4: parametric tables) for
+// element format DT.  With a slot area, modes 0, 2, 3 and 4 code with the
+// warp-specialised compressor; without one (the allocation-free entry point,
+// modes 0 to 3 only) the one-warp compressor codes.
 template <int DT>
 cudaError_t launch_mode(CompressArgs a, int mode, bool stash, cudaStream_t s) {
     cudaError_t err;
@@ -1276,8 +1282,13 @@ cudaError_t launch_mode(CompressArgs a, int mode, bool stash, cudaStream_t s) {
         raw_kernel<DT><<<dim3(uint32_t(grid)), dim3(32), 0, s>>>(a);
         if ((err = cudaGetLastError()) != cudaSuccess || mode == 1) return err;
     }
-    if ((mode == 0 || mode == 2) && stash && C > 0) return launch_ws<DT, false>(a, s);
-    if (mode == 3 && stash && C > 0) return launch_ws<DT, true>(a, s);
+    if ((mode == 0 || mode == 2) && stash && C > 0) return launch_ws<DT, 0>(a, s);
+    if (mode == 3 && stash && C > 0) return launch_ws<DT, 1>(a, s);
+    if (mode == 4) {
+        if (C == 0) mode = 0;  // no chunk: the header alone
+        else if (stash) return launch_ws<DT, 2>(a, s);
+        else return cudaErrorInvalidValue;
+    }
     void (*kern)(CompressArgs) = mode == 3 ? compress_kernel<DT, true> : compress_kernel<DT, false>;
     if ((err = launch_shape(reinterpret_cast<const void*>(kern), 32, kCompressSmem, &sms, &per_sm)) != cudaSuccess)
         return err;

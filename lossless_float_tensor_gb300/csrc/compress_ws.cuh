@@ -111,7 +111,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 // bytes leave as 16-byte stores; every exponent increments row e, column
 // lane mod 16 of the histogram (red.shared).  CM 2 (sampled tables): only the
 // exponents at positions 0, 16, 32, ... of the chunk are counted, i.e. each
-// unit's first.
+// unit's first; CM 0 (parametric tables): none.
 template <int DT, int CM = 1>
 __device__ void ws_split_bytes(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* __restrict__ rem_dst,
                                uint8_t* __restrict__ ex_dst, uint32_t hist_s, uint32_t lane, uint64_t pol) {
@@ -132,7 +132,7 @@ __device__ void ws_split_bytes(const uint8_t* __restrict__ cin, uint32_t n_c, ui
                 const uint32_t sg = prmt(a, b, 0xFDB9);  // high bytes, sign replicated
                 r[g] = (lo & 0x7F7F7F7Fu) | (sg & 0x80808080u);
                 ex[g] = prmt(a << 1, b << 1, 0x7531);
-                if (CM == 1 || g == 0) red_shared_inc(hist_s + (((a >> 1) & 0x3FC0u) | lane4));
+                if (CM == 1 || (CM == 2 && g == 0)) red_shared_inc(hist_s + (((a >> 1) & 0x3FC0u) | lane4));
                 if (CM == 1) {
                     red_shared_inc(hist_s + (((a >> 17) & 0x3FC0u) | lane4));
                     red_shared_inc(hist_s + (((b >> 1) & 0x3FC0u) | lane4));
@@ -155,7 +155,7 @@ __device__ void ws_split_bytes(const uint8_t* __restrict__ cin, uint32_t n_c, ui
                 r[3 * g] = prmt(prmt(a, t, 0x0410), b, 0x4210);      // a0 a1 t0 b0
                 r[3 * g + 1] = prmt(prmt(b, t, 0x0051), c, 0x5410);  // b1 t1 c0 c1
                 r[3 * g + 2] = prmt(d, t, 0x7106);                   // t2 d0 d1 t3
-                if (CM == 1 || g == 0) red_shared_inc(hist_s + (((a >> 17) & 0x3FC0u) | lane4));
+                if (CM == 1 || (CM == 2 && g == 0)) red_shared_inc(hist_s + (((a >> 17) & 0x3FC0u) | lane4));
                 if (CM == 1) {
                     red_shared_inc(hist_s + (((b >> 17) & 0x3FC0u) | lane4));
                     red_shared_inc(hist_s + (((c >> 17) & 0x3FC0u) | lane4));
@@ -205,7 +205,7 @@ __device__ void ws_split_bytes(const uint8_t* __restrict__ cin, uint32_t n_c, ui
         const uint32_t e = Traits<DT>::exp_of(b);
 #pragma unroll
         for (uint32_t k = 0; k < es - 1; ++k) rem_dst[(es - 1) * uint64_t(i) + k] = uint8_t(r >> (8 * k));
-        if (CM == 1 || (i & 15u) == 0) red_shared_inc(hist_s + ((e << 6) | lane4));
+        if (CM == 1 || (CM == 2 && (i & 15u) == 0)) red_shared_inc(hist_s + ((e << 6) | lane4));
         ex_dst[i] = uint8_t(e);
     }
 }
@@ -213,7 +213,7 @@ __device__ void ws_split_bytes(const uint8_t* __restrict__ cin, uint32_t n_c, ui
 // The same pass for formats whose sign|fraction field is not a whole number
 // of bytes (fp16: 11 bits, fp8 e4m3fn: 4, e5m2: 3): a unit is 32 values, whose
 // W-bit fields pack into exactly W 32-bit words, least significant bit first.
-// CM 2: only the unit's values 0 and 16 are counted.
+// CM 2: only the unit's values 0 and 16 are counted; CM 0: none.
 template <int DT, int CM = 1>
 __device__ void ws_split_packed(const uint8_t* __restrict__ cin, uint32_t n_c, uint8_t* __restrict__ rem_dst,
                                 uint8_t* __restrict__ ex_dst, uint32_t hist_s, uint32_t lane, uint64_t pol) {
@@ -233,7 +233,7 @@ __device__ void ws_split_packed(const uint8_t* __restrict__ cin, uint32_t n_c, u
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const uint32_t eb = (w[j] >> mb) & em2;  // both exponents, bytes 0 and 2
-                if (CM == 1 || j == 0 || j == 8) count((eb << 6) & 0x3FC0u);
+                if (CM == 1 || (CM == 2 && (j == 0 || j == 8))) count((eb << 6) & 0x3FC0u);
                 if (CM == 1) count((eb >> 10) & 0x3FC0u);
                 f[2 * j] = Traits<DT>::rem_of(w[j] & 0xFFFFu);
                 f[2 * j + 1] = Traits<DT>::rem_of(w[j] >> 16);
@@ -244,7 +244,7 @@ __device__ void ws_split_packed(const uint8_t* __restrict__ cin, uint32_t n_c, u
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 ex[j] = (w[j] >> mb) & em4;
-                if (CM == 1 || j == 0 || j == 4) count((ex[j] << 6) & 0x3FC0u);
+                if (CM == 1 || (CM == 2 && (j == 0 || j == 4))) count((ex[j] << 6) & 0x3FC0u);
                 if (CM == 1) {
                     count((ex[j] >> 2) & 0x3FC0u);
                     count((ex[j] >> 10) & 0x3FC0u);
@@ -316,7 +316,7 @@ __device__ void ws_split_packed(const uint8_t* __restrict__ cin, uint32_t n_c, u
         }
         for (uint32_t i = i0 + lane; i < n_c; i += 32) {
             const uint32_t e = Traits<DT>::exp_of(Traits<DT>::load(cin, i));
-            if (CM == 1 || (i & 15u) == 0) count(e << 6);
+            if (CM == 1 || (CM == 2 && (i & 15u) == 0)) count(e << 6);
             ex_dst[i] = uint8_t(e);
         }
     }
@@ -394,10 +394,8 @@ __device__ uint32_t ws_direct(const uint8_t* __restrict__ cin, uint32_t n_c, uin
     x = kRansL;
     uint32_t cnt = 0;
     int32_t pos = int32_t(W);
-    for (int32_t t = int32_t((n_c + 31) / 32) - 1; t >= 0; --t) {
-        const uint32_t i = 32 * uint32_t(t) + lane;
-        const bool active = i < n_c;
-        const uint32_t e = active ? Traits<DT>::exp_of(Traits<DT>::load(cin, i)) : 0u;
+    auto step = [&](int32_t t, uint32_t e) {
+        const bool active = 32 * uint32_t(t) + lane < n_c;
         uint32_t mlo, pk;
         asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(mlo), "=r"(pk) : "r"(table_s + 8 * e));
         const bool emit = active && x > (~pk | 0xFFFFFu);
@@ -410,6 +408,22 @@ __device__ uint32_t ws_direct(const uint8_t* __restrict__ cin, uint32_t n_c, uin
         const uint32_t q = __funnelshift_r(__umulhi(xr, mlo) + xr, 0u, pk);
         const uint32_t xn = q * (pk >> 20) + xr + ((pk >> 8) & 0xFFFu);
         x = active ? xn : x;
+    };
+    auto exp_at = [&](int32_t t) -> uint32_t {
+        const uint32_t i = 32 * uint32_t(t) + lane;
+        return t >= 0 && i < n_c ? Traits<DT>::exp_of(Traits<DT>::load(cin, i)) : 0u;
+    };
+    // groups of 8 steps whose input loads are issued first; the count only
+    // grows, so testing for RAW after each group decides as testing after
+    // each step would
+    constexpr int G = 8;
+    for (int32_t t0 = int32_t((n_c + 31) / 32) - 1; t0 >= 0; t0 -= G) {
+        uint32_t e[G];
+#pragma unroll
+        for (int k = 0; k < G; ++k) e[k] = exp_at(t0 - k);
+#pragma unroll
+        for (int k = 0; k < G; ++k)
+            if (t0 - k >= 0) step(t0 - k, e[k]);
         if (!WRITE && hdr + 2 * cnt >= n_c) return kRawFlag;
     }
     return cnt;
@@ -462,7 +476,7 @@ __device__ void ws_place(const CompressArgs& a, uint8_t* meta, uint8_t* ctx, uin
 // encoders' contexts in order, place the chunk the context held, wait until
 // the encoder is far enough into its other context, take the next chunk,
 // split it into the context and mark it ready.
-template <int DT, bool SAMPLED>
+template <int DT, int TM>
 __device__ void ws_helper(const CompressArgs& a, uint8_t* smem, uint32_t h, uint32_t lane) {
     const uint32_t C = a.num_chunks;
     const uint32_t processed = C - a.first_ticket;
@@ -521,22 +535,28 @@ __device__ void ws_helper(const CompressArgs& a, uint8_t* smem, uint32_t h, uint
         const uint64_t left = a.n - uint64_t(c) * kChunk;
         const uint32_t n_c = uint32_t(left < kChunk ? left : kChunk);
         const uint8_t* cin = a.in + uint64_t(c) * kChunk * Fmt<DT>::kEs;
-        {
+        if constexpr (TM != 2) {  // the histogram the split counts into
             const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll 8
             for (uint32_t i = lane; i < kWsHist / 16; i += 32) reinterpret_cast<uint4*>(hsm)[i] = z;
         }
         __syncwarp();
         uint8_t* rem_dst = a.out + rem_off + uint64_t(c) * Fmt<DT>::kRemChunk;
-        if constexpr (Fmt<DT>::kPacked) ws_split_packed<DT, SAMPLED ? 2 : 1>(cin, n_c, rem_dst, ctx, hist_s, lane, pol);
-        else ws_split_bytes<DT, SAMPLED ? 2 : 1>(cin, n_c, rem_dst, ctx, hist_s, lane, pol);
+        constexpr int CM = TM == 0 ? 1 : (TM == 1 ? 2 : 0);  // which exponents the histogram counts
+        if constexpr (Fmt<DT>::kPacked) ws_split_packed<DT, CM>(cin, n_c, rem_dst, ctx, hist_s, lane, pol);
+        else ws_split_bytes<DT, CM>(cin, n_c, rem_dst, ctx, hist_s, lane, pol);
         __syncwarp();
         if (a.progress) post_progress(a.progress + 2 * uint64_t(c), 1, lane);
         uint32_t cnt[8];
-        reduce_hist(hsm, lane, cnt);
+        if constexpr (TM != 2) reduce_hist(hsm, lane, cnt);
         Norm nm;
         uint32_t total = n_c;  // the counts' total
-        if constexpr (SAMPLED) {  // a seen symbol counts 16 x, an unseen one of the format's range 1
+        if constexpr (TM == 2) {  // the model's counts, the same for every chunk
+#pragma unroll
+            for (int k = 0; k < 8; ++k) cnt[k] = a.model[8 * lane + k];
+            total = a.model_total;
+        }
+        if constexpr (TM == 1) {  // a seen symbol counts 16 x, an unseen one of the format's range 1
             uint32_t part = 0;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -548,7 +568,7 @@ __device__ void ws_helper(const CompressArgs& a, uint8_t* smem, uint32_t h, uint
             for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
             total = part;
         }
-        normalise<SAMPLED>(cnt, total, lane, regB, nm);
+        normalise<TM != 0>(cnt, total, lane, regB, nm);
         ws_build_table(nm, lane, table_s, meta);
         if (lane == 0) {
             *reinterpret_cast<volatile uint32_t*>(meta + kMetaChunk) = c;
@@ -819,7 +839,7 @@ __device__ void ws_encoder(const CompressArgs& a, uint8_t* smem, uint32_t e, uin
     }
 }
 
-template <int DT, bool SAMPLED>
+template <int DT, int TM>
 __global__ void __launch_bounds__(kWsThreads, 1) compress_ws_kernel(CompressArgs a) {
     extern __shared__ __align__(128) uint8_t ws_smem[];
     uint8_t* smem = ws_smem;
@@ -834,12 +854,12 @@ __global__ void __launch_bounds__(kWsThreads, 1) compress_ws_kernel(CompressArgs
     }
     __syncthreads();
     if (warp < kWsEnc) ws_encoder<DT>(a, smem, warp, lane);
-    else ws_helper<DT, SAMPLED>(a, smem, warp - kWsEnc, lane);
+    else ws_helper<DT, TM>(a, smem, warp - kWsEnc, lane);
 }
 
-template <int DT, bool SAMPLED>
+template <int DT, int TM>
 cudaError_t launch_ws(const CompressArgs& a, cudaStream_t s) {
-    void (*kern)(CompressArgs) = compress_ws_kernel<DT, SAMPLED>;
+    void (*kern)(CompressArgs) = compress_ws_kernel<DT, TM>;
     cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, int(kWsSmem));
     if (err != cudaSuccess) return err;

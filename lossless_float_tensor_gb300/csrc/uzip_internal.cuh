@@ -333,14 +333,19 @@ cudaError_t launch_shape(const void* kern, int threads, size_t smem, int* sms, i
 // launchers (compress.cu, decompress.cu, pipeline.cu)
 // mode: 0 per-chunk choice, 1 whole message RAW, 2 gated (a one-warp kernel
 // decides from the first 64 KiB of input), 3 per-chunk choice with sampled
-// tables
+// tables, 4 per-chunk choice with the one table of the model counts `model`
+// (256 u32, see model_counts)
 // progress (nullable, mapped host memory, 2 u64 per chunk): see CompressArgs
 cudaError_t launch_compress(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                             int32_t* d_status, uint32_t first_ticket, cudaStream_t s, int mode = 0,
-                            uint64_t* progress = nullptr);
+                            uint64_t* progress = nullptr, const uint32_t* model = nullptr);
 cudaError_t launch_compress_with_scratch(int dtype, const void* d_in, uint64_t n, void* d_out, uint64_t* d_out_size,
                                          int32_t* d_status, uint32_t first_ticket, void* scratch_area, void* stash,
-                                         cudaStream_t s, int mode = 0, uint64_t* progress = nullptr);
+                                         cudaStream_t s, int mode = 0, uint64_t* progress = nullptr,
+                                         const uint32_t* model = nullptr);
+// Gaussian-model counts (mode 4) for values ~ N(0, sigma^2) (compress.cu);
+// false for a sigma that is not finite and positive
+bool model_counts(int dtype, double sigma, uint32_t counts[256]);
 
 // warp-specialised compressor: blocks of its encoder's current chunk left when
 // a helper starts splitting the next one (compress.cu; a test hook sets it)

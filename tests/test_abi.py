@@ -160,3 +160,27 @@ def test_binding_constants_match_the_header(uz):
     for name, value in re.findall(r"\b(UZIP_[A-Z0-9_]+)\s*=\s*(\d+)", text):
         if hasattr(uz, name):
             assert getattr(uz, name) == int(value), name
+
+
+@pytest.mark.parametrize("dtype", [0, 1, 2, 3, 4])
+def test_parametric_model_counts_equal_the_oracle(uz, dtype):
+    """The library's host code and the oracle compute the Gaussian-model
+    counts independently from one definition; they agree to the bit."""
+    import ctypes
+
+    import numpy as np
+
+    for sigma in [1e-6, 3e-4, 0.02, 0.1234, 0.7, 1.0, 5.5, 300.0, 2.0 ** 40]:
+        got = (ctypes.c_uint32 * 256)()
+        assert uz.library().uzip_debug_model_counts(dtype, sigma, got) == 1
+        want, _ = oracle.parametric_counts(dtype, sigma)
+        assert np.array_equal(np.frombuffer(got, np.uint32), want), sigma
+    for bad in [0.0, -0.5, float("inf"), float("nan")]:
+        assert uz.library().uzip_debug_model_counts(dtype, bad, (ctypes.c_uint32 * 256)()) == 0
+
+
+def test_parametric_refuses_bad_sigma_before_any_work(uz):
+    fake = 1 << 40  # aligned, never dereferenced
+    for bad in [0.0, -1.0, float("inf"), float("nan")]:
+        assert uz.uzip_compress_parametric(fake, 0, 10, fake, 1 << 30, None, None, bad, 0) == uz.UZIP_ERR_INVALID_ARG
+    assert uz.uzip_compress_parametric(fake, 5, 10, fake, 1 << 30, None, None, 1.0, 0) == uz.UZIP_ERR_UNSUPPORTED_DTYPE
