@@ -622,8 +622,10 @@ def run_gate(args, dev, x, n, peak):
     sample codes, so the gated call costs the gate kernel on top of the usual
     compression; on 1 GiB of random bf16 bits the sample goes RAW and the
     whole message is split and stored RAW without statistics or coding.  Also
-    c4 with tables from a sample of each chunk (UZIP_FLAG_SAMPLED_TABLES).
-    CUDA events, mean of 5 launches after 3 warm-ups."""
+    the other table modes: tables from a sample of each chunk
+    (UZIP_FLAG_SAMPLED_TABLES) and one Gaussian-model table for every chunk
+    (uzip_compress_parametric), on c4 and on c5 message 0.  CUDA events, mean
+    of 5 launches after 3 warm-ups."""
     import numpy as np
     import torch
 
@@ -667,17 +669,42 @@ def run_gate(args, dev, x, n, peak):
     rows["random_gated_bytes"] = int(size.item())
     rows["raw_frac_of_hbm"] = (4 * n) / (rows["random_gated_ms"] / 1e3) / 1e9 / peak
 
-    def run_sampled():
-        st = uz.uzip_compress_ex(x.data_ptr(), uz.UZIP_BF16, n, comp.data_ptr(), cap, size.data_ptr(), None,
+    def run_sampled(t):
+        st = uz.uzip_compress_ex(t.data_ptr(), uz.UZIP_BF16, n, comp.data_ptr(), cap, size.data_ptr(), None,
                                  uz.UZIP_FLAG_SAMPLED_TABLES, sp)
         if st:
             raise RuntimeError(f"uzip status {st}")
 
-    rows["c4_sampled_tables_ms"] = timed(run_sampled)
+    rows["c4_sampled_tables_ms"] = timed(lambda: run_sampled(x))
     rows["c4_sampled_tables_bytes"] = int(size.item())
     del rnd
-    return {"workload": "c4 (1 GiB bf16) and 1 GiB of random bf16 bits (numpy seed 17)", "unit": "ms per launch",
-            **rows}
+
+    def run_model(t, sigma):
+        st = uz.uzip_compress_parametric(t.data_ptr(), uz.UZIP_BF16, n, comp.data_ptr(), cap, size.data_ptr(), None,
+                                         sigma, sp)
+        if st:
+            raise RuntimeError(f"uzip status {st}")
+
+    # Gaussian-model tables: c4 under its standard deviation (0.5 t(4):
+    # 0.5 sqrt 2), and c5 message 0 (N(0, 0.02), which the model fits) in all
+    # three table modes
+    rows["c4_parametric_ms"] = timed(lambda: run_model(x, 0.5 * 2 ** 0.5))
+    rows["c4_parametric_bytes"] = int(size.item())
+    import synth
+
+    m0 = synth.c5_message(0)
+    if m0.size == n:
+        g = torch.from_numpy(m0.view(np.int16)).to(dev)
+        del m0
+        rows["c5m0_full_ms"] = timed(lambda: run(g))
+        rows["c5m0_full_bytes"] = int(size.item())
+        rows["c5m0_sampled_tables_ms"] = timed(lambda: run_sampled(g))
+        rows["c5m0_sampled_tables_bytes"] = int(size.item())
+        rows["c5m0_parametric_ms"] = timed(lambda: run_model(g, 0.02))
+        rows["c5m0_parametric_bytes"] = int(size.item())
+        del g
+    return {"workload": "c4 (1 GiB bf16), 1 GiB of random bf16 bits (numpy seed 17), c5 message 0 (1 GiB bf16)",
+            "unit": "ms per launch", **rows}
 
 
 def run_dtype_sweep(args, dev, peak):
