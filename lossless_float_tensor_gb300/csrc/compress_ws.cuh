@@ -21,6 +21,12 @@
 // Sec. IV-C).  A helper starts splitting an encoder's next chunk only once the
 // encoder is well into its current one, so few contexts are held in L2 at a
 // time.
+//
+// Table modes (template parameter TM): 0 counts every exponent of the chunk;
+// 1 counts those at positions 0, 16, 32, ... and normalises 16 x the sample
+// counts, every unseen symbol of the format's range counting 1; 2 counts
+// nothing and normalises the caller's Gaussian-model counts (ZipCCL
+// abstract), the same for every chunk.
 #pragma once
 
 #include "compress_kernels.cuh"
