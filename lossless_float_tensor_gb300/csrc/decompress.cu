@@ -291,6 +291,10 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
         const uint32_t nlines = (len + 15) / 16;
         const uint32_t npieces = (nlines + 15) / 16;
         const bool half = lane < 16;                      // a piece is 16 lines: lanes 0..15
+        // steps between top-ups: their worst case plus a partly read piece and
+        // the piece in flight fill the four slots exactly
+        constexpr int kPeriod = 8;
+        static_assert(2 * kPeriod * kLanes + 2 * 256 <= 1024, "the ring holds one period past pos");
         auto load_piece = [&](uint32_t piece) -> uint4 {
             const uint32_t line = piece * 16 + (lane & 15);
             uint4 v = make_uint4(0, 0, 0, 0);
@@ -313,7 +317,7 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
             has_pend = false;
             pos = (rq - wb0) >> 1;
             const uint32_t cur = (wb0 + 2 * pos) >> 8;
-            uint32_t need_end = ((wb0 + 2 * (pos + 8 * 32)) >> 8) + 1;
+            uint32_t need_end = ((wb0 + 2 * (pos + kPeriod * kLanes)) >> 8) + 1;
             need_end = need_end < npieces ? need_end : npieces;
             while (next_piece < need_end) {  // behind: bring pieces in now
                 store_piece(next_piece, load_piece(next_piece));
@@ -362,7 +366,8 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
                 if (at < nlines * 16) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + at));
             }
         };
-        constexpr int PF = 8;
+        constexpr int PF = kPeriod;  // one remainder field per step and top-up period in flight
+        static_assert(kSteps % (2 * PF) == 0, "the remainder prefetch walks whole pairs of PF steps");
         uint32_t ra[PF], rbk[PF];
 #pragma unroll
         for (int j = 0; j < PF; ++j) ra[j] = load_rem_full(j);
@@ -399,6 +404,7 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
             }
         };
         constexpr int PF = DT == UZIP_BF16 ? 16 : 8;
+        static_assert(kSteps % (2 * PF) == 0, "the remainder prefetch walks whole pairs of PF steps");
         uint32_t ra[PF], rbk[PF];
 #pragma unroll
         for (int j = 0; j < PF; ++j) ra[j] = load_rem_full(j);
