@@ -469,50 +469,147 @@ def run_configs(args, dev, peak, x4, bits4, c5_msgs):
 
 
 def run_e2e(args, x, bits, comp, cap, size, out, status, stream, dev, total):
-    """H2D of the input from pinned memory, compress, D2H of the container,
-    H2D of the container, decompress, D2H of the output, every step."""
+    """End to end through the public API with host buffers.  Every step: H2D
+    of the input from pinned memory, compress, D2H of the container (its
+    exact size read on the host), H2D of the container, decompress, D2H of
+    the output.  Steps run back to back as a two-slot software pipeline on
+    three streams (uploads, kernels, downloads): the host link carries both
+    directions at once, so step k's container and output travel down while
+    step k + 1's input and step k's container travel up.  A buffer a step
+    writes is written again two steps later, after an event says its last
+    reader is done.  The same chain run one step at a time on one stream is
+    reported beside it ("serial_gbs")."""
     import numpy as np
     import torch
 
     import lossless_float_tensor_gb300 as uz
 
     n = bits.size
+    S = 2
     h_in = torch.from_numpy(bits.view(np.int16)).pin_memory()
-    h_comp = torch.empty(cap, dtype=torch.uint8).pin_memory()
-    h_out = torch.empty(n, dtype=torch.int16).pin_memory()
-    h_size = torch.zeros((), dtype=torch.int64).pin_memory()
-    d_in = torch.empty(n, dtype=torch.int16, device=dev)
-    d_comp2 = torch.empty(cap, dtype=torch.uint8, device=dev)
-    sp = stream.cuda_stream
-    steps = max(1, min(args.steps, 5))
+    h_comp = [torch.empty(cap, dtype=torch.uint8).pin_memory() for _ in range(S)]
+    h_out = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(S)]
+    h_size = torch.zeros(S, dtype=torch.int64).pin_memory()
+    d_in = [torch.empty(n, dtype=torch.int16, device=dev) for _ in range(S)]
+    d_comp = [comp, torch.empty(cap, dtype=torch.uint8, device=dev)]
+    d_size = [size, torch.zeros((), dtype=torch.int64, device=dev)]
+    d_comp2 = [torch.empty(cap, dtype=torch.uint8, device=dev) for _ in range(S)]
+    d_out = [out.view(torch.int16), torch.empty(n, dtype=torch.int16, device=dev)]
+    d_status = [status, torch.zeros((), dtype=torch.int32, device=dev)]
+    up, ks, down = torch.cuda.Stream(dev), stream, torch.cuda.Stream(dev)
+    ev = [{k: torch.cuda.Event() for k in ("in", "comp", "cdn", "cup", "dec", "odn")} for _ in range(S)]
+    tb = [0] * S
 
-    def one():
-        with torch.cuda.stream(stream):
-            d_in.copy_(h_in, non_blocking=True)
-            st = uz.uzip_compress(d_in.data_ptr(), uz.UZIP_BF16, n, comp.data_ptr(), cap, size.data_ptr(), sp)
-            h_size.copy_(size, non_blocking=True)
-        stream.synchronize()
-        tb = int(h_size.item())
-        with torch.cuda.stream(stream):
-            h_comp[:tb].copy_(comp[:tb], non_blocking=True)
-            d_comp2[:tb].copy_(h_comp[:tb], non_blocking=True)
-            st2 = uz.uzip_decompress(d_comp2.data_ptr(), tb, out.data_ptr(), uz.UZIP_BF16, n, status.data_ptr(), sp)
-            h_out.copy_(out.view(torch.int16), non_blocking=True)
-        stream.synchronize()
+    def encode(k):  # input up, compress
+        b, e = k % S, ev[k % S]
+        if k >= S:
+            up.wait_event(e["comp"])  # compression k - 2 has read d_in[b]
+        with torch.cuda.stream(up):
+            d_in[b].copy_(h_in, non_blocking=True)
+        e["in"].record(up)
+        ks.wait_event(e["in"])
+        if k >= S:
+            ks.wait_event(e["cdn"])  # container k - 2 has left d_comp[b]
+        with torch.cuda.stream(ks):
+            st = uz.uzip_compress(d_in[b].data_ptr(), uz.UZIP_BF16, n, d_comp[b].data_ptr(), cap,
+                                  d_size[b].data_ptr(), ks.cuda_stream)
+            h_size[b].copy_(d_size[b], non_blocking=True)
+        e["comp"].record(ks)
+        if st:
+            raise RuntimeError(f"e2e compress status {st}")
+
+    def container_down(k):  # the host reads the size, then the container goes down
+        b, e = k % S, ev[k % S]
+        e["comp"].synchronize()
+        tb[b] = int(h_size[b])
+        if tb[b] <= 0:
+            raise RuntimeError("e2e compress failed")
+        down.wait_event(e["comp"])
+        if k >= S:
+            down.wait_event(e["cup"])  # container k - 2 has left h_comp[b]
+        with torch.cuda.stream(down):
+            h_comp[b][:tb[b]].copy_(d_comp[b][:tb[b]], non_blocking=True)
+        e["cdn"].record(down)
+
+    def decode(k):  # container up, decompress
+        b, e = k % S, ev[k % S]
+        up.wait_event(e["cdn"])
+        if k >= S:
+            up.wait_event(e["dec"])  # decompression k - 2 has read d_comp2[b]
+        with torch.cuda.stream(up):
+            d_comp2[b][:tb[b]].copy_(h_comp[b][:tb[b]], non_blocking=True)
+        e["cup"].record(up)
+        ks.wait_event(e["cup"])
+        if k >= S:
+            ks.wait_event(e["odn"])  # output k - 2 has left d_out[b]
+        with torch.cuda.stream(ks):
+            st = uz.uzip_decompress(d_comp2[b].data_ptr(), tb[b], d_out[b].data_ptr(), uz.UZIP_BF16, n,
+                                    d_status[b].data_ptr(), ks.cuda_stream)
+        e["dec"].record(ks)
+        if st:
+            raise RuntimeError(f"e2e decompress status {st}")
+
+    def output_down(k):
+        b, e = k % S, ev[k % S]
+        down.wait_event(e["dec"])
+        with torch.cuda.stream(down):
+            h_out[b].copy_(d_out[b], non_blocking=True)
+        e["odn"].record(down)
+
+    def pipelined(steps):
+        # per period the uplink carries input k and container k - 1, the
+        # downlink container k and output k - 1, in that order
+        for k in range(steps + 1):
+            if k < steps:
+                encode(k)
+            if k >= 1:
+                decode(k - 1)
+            if k < steps:
+                container_down(k)
+            if k >= 1:
+                output_down(k - 1)
+        torch.cuda.synchronize(dev)
+
+    def serial():
+        b = 0
+        with torch.cuda.stream(ks):
+            d_in[b].copy_(h_in, non_blocking=True)
+            st = uz.uzip_compress(d_in[b].data_ptr(), uz.UZIP_BF16, n, d_comp[b].data_ptr(), cap,
+                                  d_size[b].data_ptr(), ks.cuda_stream)
+            h_size[b].copy_(d_size[b], non_blocking=True)
+        ks.synchronize()
+        t = int(h_size[b])
+        with torch.cuda.stream(ks):
+            h_comp[b][:t].copy_(d_comp[b][:t], non_blocking=True)
+            d_comp2[b][:t].copy_(h_comp[b][:t], non_blocking=True)
+            st2 = uz.uzip_decompress(d_comp2[b].data_ptr(), t, d_out[b].data_ptr(), uz.UZIP_BF16, n,
+                                     d_status[b].data_ptr(), ks.cuda_stream)
+            h_out[b].copy_(d_out[b], non_blocking=True)
+        ks.synchronize()
         if st or st2:
             raise RuntimeError("e2e status")
-        return tb
+        return t
 
-    one()
-    torch.cuda.synchronize(dev)
+    steps = max(2, min(args.steps, 10))
+    pipelined(2)  # warm-up
+    for h in h_out:
+        h.zero_()
     t0 = time.perf_counter()
-    tb = 0
-    for _ in range(steps):
-        tb = one()
+    pipelined(steps)
     dt = (time.perf_counter() - t0) / steps
-    ok = bool(np.array_equal(h_out.numpy().view(np.uint16), bits))
-    return {"value": 2 * n / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": 2 * n + tb,
-            "d2h_bytes_per_step": tb + 2 * n + 8, "steps": steps, "bit_exact": ok}
+    ok = all(bool(np.array_equal(h.numpy().view(np.uint16), bits)) for h in h_out)
+    ok = ok and all(int(s_.item()) == 0 for s_ in d_status) and tb[0] == tb[1]
+    serial()
+    t0 = time.perf_counter()
+    ts = 0
+    for _ in range(3):
+        ts = serial()
+    dts = (time.perf_counter() - t0) / 3
+    ok = ok and ts == tb[0] and bool(np.array_equal(h_out[0].numpy().view(np.uint16), bits))
+    return {"value": 2 * n / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": 2 * n + tb[0],
+            "d2h_bytes_per_step": tb[0] + 2 * n + 8, "steps": steps, "bit_exact": ok,
+            "schedule": "two-slot pipeline over steps: uploads, kernels and downloads on three streams",
+            "serial_gbs": 2 * n / dts / 1e9}
 
 
 def run_pipeline(args, dev):
