@@ -243,7 +243,80 @@ CONFIG_LABELS = {
     "c3": "268,435,456 fp32 gradients with specials (1 GiB)",
     "c4": "[8, 8192, 8192] bf16 activations, 0.5*t(4), outliers x50, one random chunk (1 GiB)",
     "c5m0": "c5 message 0: first 1 GiB of the Llama-3-8B-shaped parameter set, bf16 ~ N(0, 0.02)",
+    "c2_streams": "c2's 7 calls issued at once on 7 streams (one call per tensor, buffers of their own); L2 flushed",
 }
+
+
+def measure_concurrent(name, dtype, arrays, dev, peak, oracle_config):
+    """The tensors of a workload compressed (then decompressed) by one call
+    each, all calls issued at once on a stream per tensor: CUDA events from
+    a start event every stream waits on to the last stream's end, mean of 5
+    rounds after 3 warm-ups, L2 flushed before each timed round; plus the
+    container hashes (the same bytes as one call at a time) and a bit-exact
+    round-trip check."""
+    import hashlib
+
+    import numpy as np
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+
+    main = torch.cuda.Stream(dev)
+    streams = [torch.cuda.Stream(dev) for _ in arrays]
+    scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    xs = [torch.from_numpy(np.ascontiguousarray(b).view(np.uint8)).to(dev) for b in arrays]
+    ns = [b.size for b in arrays]
+    caps = [uz.uzip_max_compressed_size(dtype, n) for n in ns]
+    comps = [torch.empty(c, dtype=torch.uint8, device=dev) for c in caps]
+    sizes = [torch.zeros((), dtype=torch.int64, device=dev) for _ in arrays]
+    outs = [torch.empty_like(x) for x in xs]
+    stats = [torch.zeros((), dtype=torch.int32, device=dev) for _ in arrays]
+    torch.cuda.synchronize(dev)
+
+    def round_(launch):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        done = [torch.cuda.Event() for _ in streams]
+        with torch.cuda.stream(main):
+            scrub.fill_(7)
+        t0.record(main)
+        for i, st in enumerate(streams):
+            st.wait_event(t0)
+            with torch.cuda.stream(st):
+                if launch(i, st.cuda_stream):
+                    raise RuntimeError(f"{name}: uzip status")
+            done[i].record(st)
+        for d in done:
+            main.wait_event(d)
+        t1.record(main)
+        return t0, t1
+
+    def comp(i, sp):
+        return uz.uzip_compress(xs[i].data_ptr(), dtype, ns[i], comps[i].data_ptr(), caps[i], sizes[i].data_ptr(), sp)
+
+    def dec(i, sp):
+        return uz.uzip_decompress(comps[i].data_ptr(), caps[i], outs[i].data_ptr(), dtype, ns[i], stats[i].data_ptr(),
+                                  sp)
+
+    tc, td = [], []
+    for k in range(8):
+        ec = round_(comp)
+        ed = round_(dec)
+        if k >= 3:
+            tc.append(ec)
+            td.append(ed)
+    torch.cuda.synchronize(dev)
+    mc = statistics.mean(a.elapsed_time(b) for a, b in tc) / 1e3
+    md = statistics.mean(a.elapsed_time(b) for a, b in td) / 1e3
+    tots = [int(s_.item()) for s_ in sizes]
+    exact = all(int(s_.item()) == 0 for s_ in stats) and all(torch.equal(o, x) for o, x in zip(outs, xs))
+    hashes = [hashlib.sha256(c[:t].cpu().numpy().tobytes()).hexdigest() for c, t in zip(comps, tots)]
+    nbytes, total = sum(b.nbytes for b in arrays), sum(tots)
+    moved = nbytes + total
+    return {"config": name, "workload": CONFIG_LABELS[name], "input_bytes": nbytes, "compressed_bytes": total,
+            "ratio": total / nbytes, "compress_ms": mc * 1e3, "decompress_ms": md * 1e3,
+            "compress_gbs": nbytes / mc / 1e9, "decompress_gbs": nbytes / md / 1e9,
+            "compress_frac": moved / mc / 1e9 / peak, "decompress_frac": moved / md / 1e9 / peak,
+            "round_trip_exact": bool(exact), "sha256": hashes, "oracle_config": oracle_config}
 
 
 def measure_config(name, dtype, arrays, dev, peak, flush_l2):
@@ -418,7 +491,7 @@ def run_ours(args, rank, world, local_rank):
                "compress_gbs": c4r["compress_gbs"], "decompress_gbs": c4r["decompress_gbs"], **host_description()}
         if configs is not None:
             for row in configs["rows"]:
-                r = results.get(row["config"])
+                r = results.get(row.get("oracle_config", row["config"]))
                 if r is not None:
                     row["oracle_compress_gbs"] = r["compress_gbs"]
                     row["oracle_decompress_gbs"] = r["decompress_gbs"]
@@ -460,6 +533,8 @@ def run_configs(args, dev, peak, x4, bits4, c5_msgs):
     for name in ["c1", "c2", "c3"]:
         dtype, arrays = config_inputs(name)
         rows.append(measure_config(name, dtype, arrays, dev, peak, flush_l2=name == "c2"))
+        if name == "c2":
+            rows.append(measure_concurrent("c2_streams", dtype, arrays, dev, peak, "c2"))
         del arrays
     rows.append(measure_config("c4", 0, [bits4], dev, peak, flush_l2=False))
     if c5_msgs is not None:

@@ -45,6 +45,12 @@
  *     the caller owns every buffer.
  *   - Calls are stream ordered and asynchronous, except uzip_query_size,
  *     which synchronises its stream.
+ *   - A call keeps all its working state in the buffers it is given (the
+ *     compressors' counters and staging in d_out, past the container), so
+ *     calls on different streams, from any host threads, may run on the GPU
+ *     at the same time as long as they share no buffer.  The one exception
+ *     is uzip_compress_noalloc, whose scratch array is shared by all its
+ *     calls on a device.
  *   - The return value reports argument and launch errors.  Data-dependent
  *     errors (a corrupt container, a device-side wait that ran out) are
  *     written to device memory (*d_status, *d_out_size = 0) and never trap.
