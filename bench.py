@@ -160,6 +160,12 @@ def replica_throughput_gbs(bytes_per_rank: int, steps: int, max_ms: float, world
     return world * bytes_per_rank * steps / (max_ms / 1e3) / 1e9
 
 
+def round_trip_gbs(input_bytes: int, compress_s: float, decompress_s: float) -> float:
+    """Input GB/s of one compress plus one decompress of input_bytes: the
+    same measure as the line's value, so the CPU baseline compares with it."""
+    return input_bytes / (compress_s + decompress_s) / 1e9
+
+
 def host_description():
     """Host cores and CPU model (x86: 'model name'; Arm: implementer/part)."""
     model, impl, part = None, None, None
@@ -484,7 +490,7 @@ def run_ours(args, rank, world, local_rank):
         oracle_pool.close()
         oracle_pool.join()
         c4r = results["c4"]
-        cpu = {"value": 2 * c4r["input_bytes"] / (c4r["compress_s"] + c4r["decompress_s"]) / 1e9, "unit": "GB/s",
+        cpu = {"value": round_trip_gbs(c4r["input_bytes"], c4r["compress_s"], c4r["decompress_s"]), "unit": "GB/s",
                "cores": 1, "kind": "oracle",
                "sample": "the whole workload (536,870,912 values), compress "
                          f"{c4r['compress_s']:.1f} s + decompress {c4r['decompress_s']:.1f} s, one thread",

@@ -44,3 +44,13 @@ def test_replica_throughput_sums_ranks():
     one = bench.replica_throughput_gbs(1 << 30, 10, 5.0, 1)
     assert one == pytest.approx((1 << 30) * 10 / 5e-3 / 1e9)
     assert bench.replica_throughput_gbs(1 << 30, 10, 5.0, 4) == pytest.approx(4 * one)
+
+
+def test_round_trip_counts_the_input_once():
+    # a round trip of B input bytes at compress rate a and decompress rate b
+    # (bytes/s) takes B/a + B/b seconds: its rate is the harmonic combination
+    b, a, d = 1 << 30, 0.165e9, 0.197e9
+    got = bench.round_trip_gbs(b, b / a, b / d)
+    assert got == pytest.approx(1 / (1 / 0.165 + 1 / 0.197))
+    # the GPU line's value uses the same measure: input bytes per round trip
+    assert bench.replica_throughput_gbs(b, 1, (b / a + b / d) * 1e3, 1) == pytest.approx(got)
