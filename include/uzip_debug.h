@@ -37,12 +37,6 @@ int uzip_debug_model_counts(int dtype, double sigma, uint32_t* counts);
  * and the L2 working set only, never the output. */
 void uzip_debug_set_ws_jit_blocks(uint32_t blocks);
 
-/* Decoder choice for the calls that follow: -1 (default) by grid size, the
- * packed-table decoder for at most 608 chunks; 0 always the byte-table
- * decoder; 1 always the packed-table decoder.  Affects speed only, never
- * the output or the verdict on a container. */
-void uzip_debug_set_decode_variant(int variant);
-
 /* Byte offset of the compressor's work area inside the output buffer (the
  * area is 16 + 8*C bytes long and follows the largest possible container). */
 uint64_t uzip_debug_scratch_offset(uzip_dtype dtype, uint64_t n);

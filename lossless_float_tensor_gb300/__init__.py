@@ -68,8 +68,6 @@ _lib.uzip_debug_div_magic.argtypes = [_u32, ctypes.POINTER(_u32), ctypes.POINTER
 _lib.uzip_debug_div_magic.restype = _int
 _lib.uzip_debug_model_counts.argtypes = [_int, ctypes.c_double, ctypes.POINTER(_u32)]
 _lib.uzip_debug_model_counts.restype = _int
-_lib.uzip_debug_set_decode_variant.argtypes = [_int]
-_lib.uzip_debug_set_decode_variant.restype = None
 _lib.uzip_debug_scratch_offset.argtypes = [_int, _u64]
 _lib.uzip_debug_scratch_offset.restype = _u64
 

@@ -277,8 +277,6 @@ int uzip_debug_div_magic33(uint32_t f, uint32_t* m_lo, uint32_t* shift) {
 
 void uzip_debug_set_ws_jit_blocks(uint32_t blocks) { g_ws_jit_blocks = blocks; }
 
-void uzip_debug_set_decode_variant(int variant) { g_dec_variant = variant < 0 ? -1 : (variant > 0 ? 1 : 0); }
-
 int uzip_debug_model_counts(int dtype, double sigma, uint32_t* counts) {
     if (!counts || !valid_dtype(dtype)) return 0;
     return model_counts(dtype, sigma, counts) ? 1 : 0;

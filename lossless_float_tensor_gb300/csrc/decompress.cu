@@ -9,8 +9,6 @@
 
 namespace uzip {
 
-int g_dec_variant = -1;
-
 struct DecompressArgs {
     const uint8_t* comp;
     uint64_t cap;
@@ -136,17 +134,13 @@ __device__ void merge_raw_packed(const uint8_t* __restrict__ ex, const uint8_t* 
 // checked that the stream padded to 16 bytes lies inside the readable buffer,
 // so full chunks may stage the word stream through shared memory in 16-byte
 // lines; otherwise every word window is read from global memory.
-template <int DT, bool RING, bool PACKED>
+template <int DT, bool RING>
 __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, const uint8_t* __restrict__ rem,
                              uint8_t* __restrict__ out, uint32_t n_c, uint32_t lane, uint8_t* wsm) {
     constexpr uint32_t es = Fmt<DT>::kEs;
     uint8_t* slot_sym = wsm;                                                   // u8[4096]
     uint2* sym_gc = reinterpret_cast<uint2*>(wsm + kDecSlotTable);                  // {f - 4096, -cum}
-    uint32_t* plist = reinterpret_cast<uint32_t*>(                                  // u32[256]: cum << 8 | s
-        wsm + (PACKED ? kDecPackedTable : kDecSlotTable + kDecSymTable));
-    // a full chunk staged through the ring, in the packed-table kernel: one
-    // u32 per slot replaces the two tables (wsm, u32[4096])
-    const bool packed = PACKED && RING && n_c == kChunk;
+    uint32_t* plist = reinterpret_cast<uint32_t*>(wsm + kDecSlotTable + kDecSymTable); // u32[256]: cum << 8 | s
     if (len < kStreamHead) return false;
     uint32_t x = reinterpret_cast<const uint32_t*>(src)[lane];
     const uint32_t bm = src[128 + lane];  // present symbols 8*lane .. 8*lane+7
@@ -184,39 +178,8 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
         }
     }
     __syncwarp();
-    if (packed) {
-        // lane fills slots [128 lane, 128 lane + 128), four per 16-byte store:
-        // (f - 1) << 20 | s << 12 | (slot - cum) for the symbol s whose slots
-        // [cum, cum + f) hold it
-        const uint32_t first = 128 * lane;
-        uint32_t lo = 0, hi = k_total - 1;
-        while (lo < hi) {
-            const uint32_t mid = (lo + hi + 1) / 2;
-            if ((plist[mid] >> 8) <= first) lo = mid;
-            else hi = mid - 1;
-        }
-        uint32_t j = lo;
-        uint32_t cur_cum = plist[j] >> 8, cur = plist[j] & 0xFFu;
-        uint32_t next_cum = j + 1 < k_total ? (plist[j + 1] >> 8) : kM;
-        const uint32_t tab_s = static_cast<uint32_t>(__cvta_generic_to_shared(wsm));
-        for (uint32_t g = 0; g < 32; ++g) {
-            const uint32_t i0 = first + 4 * g;
-            uint32_t e[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                while (next_cum <= i0 + q) {
-                    ++j;
-                    cur_cum = next_cum;
-                    cur = plist[j] & 0xFFu;
-                    next_cum = j + 1 < k_total ? (plist[j + 1] >> 8) : kM;
-                }
-                e[q] = (next_cum - cur_cum - 1) << 20 | cur << 12 | (i0 + q - cur_cum);
-            }
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(tab_s + 4 * i0), "r"(e[0]), "r"(e[1]),
-                         "r"(e[2]), "r"(e[3])
-                         : "memory");
-        }
-    } else {  // slot table: lane fills slots [128 lane, 128 lane + 128)
+    // slot table: lane fills slots [128 lane, 128 lane + 128)
+    {
         const uint32_t first = 128 * lane;
         // largest j with cum_j <= first (binary search over the sorted list)
         uint32_t lo = 0, hi = k_total - 1;
@@ -390,32 +353,6 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
             else if (es == 4) reinterpret_cast<uint32_t*>(out)[i] = v;
             else out[i] = uint8_t(v);
         };
-        // The same step from the packed table: one shared load gives f - 1,
-        // the symbol and slot - cum, and the new state is
-        // (x >> 12)(f - 1) + (x >> 12) + (slot - cum).
-        const uint32_t ptab_s = static_cast<uint32_t>(__cvta_generic_to_shared(wsm));
-        auto pstep = [&](uint32_t t, uint32_t r) {
-            const uint32_t slot = x & (kM - 1);
-            uint32_t e;
-            asm("ld.shared.u32 %0, [%1];" : "=r"(e) : "r"(ptab_s + 4 * slot));
-            const uint32_t xh = x >> kProbBits;
-            const uint32_t xn = xh * (e >> 20) + (xh + (e & 0xFFFu));
-            const bool need = xn < kRansL;
-            const uint32_t b = __ballot_sync(0xFFFFFFFFu, need);
-            uint32_t w;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=r"(w) : "r"(ring_s + ((rq + 2 * __popc(b & lt)) & 1023u)) : "memory");
-            rq += 2 * __popc(b);
-            x = need ? ((xn << 16) | w) : xn;
-            const uint32_t v = merge_fast<DT>((e >> 12) & 0xFFu, r);
-            const uint64_t i = 32 * uint64_t(t) + lane;
-            if (es == 2) reinterpret_cast<uint16_t*>(out)[i] = uint16_t(v);
-            else if (es == 4) reinterpret_cast<uint32_t*>(out)[i] = v;
-            else out[i] = uint8_t(v);
-        };
-        auto dstep = [&](uint32_t t, uint32_t r) {
-            if constexpr (PACKED) pstep(t, r);
-            else rstep(t, r);
-        };
         // Both streams are cold in L2 when decompression starts: pull the
         // remainder bytes of the steps 64 ahead and the stream bytes ~1 KiB
         // past the read position into L2 (one instruction each per 16 steps).
@@ -443,14 +380,14 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
             for (int j = 0; j < PF; ++j) rbk[j] = load_rem_full(t0 + PF + j);
             top_up();
 #pragma unroll
-            for (int j = 0; j < PF; ++j) dstep(t0 + j, ra[j]);
+            for (int j = 0; j < PF; ++j) rstep(t0 + j, ra[j]);
             if (t0 + 2 * PF < kSteps) {
 #pragma unroll
                 for (int j = 0; j < PF; ++j) ra[j] = load_rem_full(t0 + 2 * PF + j);
             }
             top_up();
 #pragma unroll
-            for (int j = 0; j < PF; ++j) dstep(t0 + PF + j, rbk[j]);
+            for (int j = 0; j < PF; ++j) rstep(t0 + PF + j, rbk[j]);
         }
         pos = (rq - wb0) >> 1;
     } else if (n_c == kChunk) {
@@ -493,12 +430,12 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
     return !__any_sync(0xFFFFFFFFu, fail);
 }
 
-template <int DT, bool PACKED>
-__global__ void __launch_bounds__(kDecWarps * 32, (PACKED ? 12 : 28) / kDecWarps) decompress_kernel(DecompressArgs a) {
+template <int DT>
+__global__ void __launch_bounds__(kDecWarps * 32, 28 / kDecWarps) decompress_kernel(DecompressArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const uint32_t lane = threadIdx.x & 31;
     const uint32_t wid = threadIdx.x >> 5;
-    uint8_t* wsm = smem + wid * (PACKED ? kDecPackedWarpSmem : kDecWarpSmem);
+    uint8_t* wsm = smem + wid * kDecWarpSmem;
     constexpr uint32_t es = Fmt<DT>::kEs;
     const uint8_t* h = a.comp;
     const uint64_t n = a.n;
@@ -539,9 +476,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, (PACKED ? 12 : 28) / kDecWarps
             } else {
                 // the ring reads the stream in whole 16-byte lines
                 if (exp_off + off + ((uint64_t(len) + 15) & ~uint64_t(15)) <= a.cap)
-                    good = decode_coded<DT, true, PACKED>(src, len, rem, out, n_c, lane, wsm);
+                    good = decode_coded<DT, true>(src, len, rem, out, n_c, lane, wsm);
                 else
-                    good = decode_coded<DT, false, PACKED>(src, len, rem, out, n_c, lane, wsm);
+                    good = decode_coded<DT, false>(src, len, rem, out, n_c, lane, wsm);
             }
         }
         if (!good && lane == 0) flag_corrupt(a.status);
@@ -555,21 +492,12 @@ cudaError_t launch_decompress(int dtype, const void* d_comp, uint64_t cap, void*
     if (d_status && (err = cudaMemsetAsync(d_status, 0, sizeof(int32_t), s)) != cudaSuccess) return err;
     DecompressArgs a{static_cast<const uint8_t*>(d_comp), cap, static_cast<uint8_t*>(d_out), n, d_status};
     const uint64_t C = num_chunks(n);  // C == 0 still launches one block to validate the header
-    // a grid too small to fill the SMs is bound by each warp's step latency:
-    // the packed table takes one shared load off the state's chain
-    const bool packed = g_dec_variant == 1 || (g_dec_variant < 0 && C <= kDecPackedMaxChunks);
-    void (*kern)(DecompressArgs) =
-        packed ? (dtype == UZIP_BF16       ? decompress_kernel<UZIP_BF16, true>
-                  : dtype == UZIP_FP32     ? decompress_kernel<UZIP_FP32, true>
-                  : dtype == UZIP_FP16     ? decompress_kernel<UZIP_FP16, true>
-                  : dtype == UZIP_FP8_E4M3 ? decompress_kernel<UZIP_FP8_E4M3, true>
-                                           : decompress_kernel<UZIP_FP8_E5M2, true>)
-               : (dtype == UZIP_BF16       ? decompress_kernel<UZIP_BF16, false>
-                  : dtype == UZIP_FP32     ? decompress_kernel<UZIP_FP32, false>
-                  : dtype == UZIP_FP16     ? decompress_kernel<UZIP_FP16, false>
-                  : dtype == UZIP_FP8_E4M3 ? decompress_kernel<UZIP_FP8_E4M3, false>
-                                           : decompress_kernel<UZIP_FP8_E5M2, false>);
-    const uint32_t smem = kDecWarps * (packed ? kDecPackedWarpSmem : kDecWarpSmem);
+    void (*kern)(DecompressArgs) = dtype == UZIP_BF16       ? decompress_kernel<UZIP_BF16>
+                                   : dtype == UZIP_FP32     ? decompress_kernel<UZIP_FP32>
+                                   : dtype == UZIP_FP16     ? decompress_kernel<UZIP_FP16>
+                                   : dtype == UZIP_FP8_E4M3 ? decompress_kernel<UZIP_FP8_E4M3>
+                                                            : decompress_kernel<UZIP_FP8_E5M2>;
+    const uint32_t smem = kDecWarps * kDecWarpSmem;
     int sms = 0, per_sm = 0;
     if ((err = launch_shape(reinterpret_cast<const void*>(kern), kDecWarps * 32, smem, &sms, &per_sm)) != cudaSuccess)
         return err;

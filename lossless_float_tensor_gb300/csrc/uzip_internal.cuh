@@ -138,15 +138,6 @@ constexpr uint32_t kDecSlotTable = 4096;    // slot -> symbol, u8[4096]
 constexpr uint32_t kDecSymTable = 2048;     // symbol -> {f - 4096, -cum}, u32 pairs[256]
 constexpr uint32_t kDecList = 1024;         // present symbols, u32[256]: cum << 8 | symbol
 constexpr uint32_t kDecWarpSmem = kDecSlotTable + kDecSymTable + kDecList;
-// the packed-table decoder for small grids: one u32 per slot,
-// (f - 1) << 20 | symbol << 12 | (slot - cum), then the symbol list (whose
-// memory is the word ring of a full chunk); partial chunks use the byte
-// tables above in the same memory
-constexpr uint32_t kDecPackedTable = 16384;
-constexpr uint32_t kDecPackedWarpSmem = kDecPackedTable + kDecList;
-// grids of at most this many chunks (four warps per SM on 152 SMs) are
-// latency-bound: they take the packed-table decoder
-constexpr uint64_t kDecPackedMaxChunks = 608;
 
 // ---- inline PTX helpers ----------------------------------------------------
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -359,9 +350,6 @@ bool model_counts(int dtype, double sigma, uint32_t counts[256]);
 // warp-specialised compressor: blocks of its encoder's current chunk left when
 // a helper starts splitting the next one (compress.cu; a test hook sets it)
 extern uint32_t g_ws_jit_blocks;
-// decoder choice (decompress.cu; a test hook sets it): -1 by grid size,
-// 0 byte tables, 1 packed table
-extern int g_dec_variant;
 
 // allocation-free compression: largest tensor and device count served by the
 // library's own work area
