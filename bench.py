@@ -8,10 +8,15 @@ channels x50 and one random-bits chunk (the 1 GiB bf16 configuration).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints one JSON line.  --impl reference times the oracle (single-threaded C)
-on a bounded sample of the same workload on the host cores.  Under torchrun
-every rank runs an independent replica (the codec has no exchange step);
-value = elements of all ranks / the slowest rank's time.
+Prints one JSON line.  value = input bytes of all ranks per round trip (one
+compress plus one decompress) / the slowest rank's time; e2e is the same
+measure through the public API from and to pinned host buffers, consecutive
+steps overlapped on upload, kernel and download streams.  The line also
+carries the per-config table, the split-send pipeline over the whole c5
+parameter set, the format sweep and the whole-message choice.  --impl
+reference times the oracle (single-threaded C) on a bounded sample of the
+same workload on the host cores.  Under torchrun every rank runs an
+independent replica (the codec has no exchange step).
 """
 from __future__ import annotations
 
