@@ -178,37 +178,58 @@ __device__ bool decode_coded(const uint8_t* __restrict__ src, uint32_t len, cons
         }
     }
     __syncwarp();
-    // slot table: lane fills slots [128 lane, 128 lane + 128)
+    // slot table in 16-slot pieces: lane l fills slots [512 g + 16 l, +16)
+    // for g = 0..7, so each 16-byte store of the warp covers 512 contiguous
+    // bytes (a lane filling one contiguous quarter-kilobyte would put all 32
+    // lanes' stores in one bank).  Each piece's first symbol comes from a
+    // branchless binary search over the sorted list (the eight searches are
+    // independent, so their loads overlap), then the piece walks forward.
     {
-        const uint32_t first = 128 * lane;
-        // largest j with cum_j <= first (binary search over the sorted list)
-        uint32_t lo = 0, hi = k_total - 1;
-        while (lo < hi) {
-            const uint32_t mid = (lo + hi + 1) / 2;
-            if ((plist[mid] >> 8) <= first) lo = mid;
-            else hi = mid - 1;
-        }
-        uint32_t j = lo;
-        uint32_t cur = plist[j] & 0xFFu;
-        uint32_t next_cum = j + 1 < k_total ? (plist[j + 1] >> 8) : kM;
-        for (uint32_t g = 0; g < 32; ++g) {
-            const uint32_t i0 = first + 4 * g;
-            uint32_t word;
-            if (next_cum > i0 + 3) {
-                word = cur * 0x01010101u;
-            } else {
-                word = 0;
+        const uint32_t first = 16 * lane;
+        uint32_t jg[8];
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    while (next_cum <= i0 + b) {
-                        ++j;
-                        cur = plist[j] & 0xFFu;
-                        next_cum = j + 1 < k_total ? (plist[j + 1] >> 8) : kM;
-                    }
-                    word |= cur << (8 * b);
-                }
+        for (int g = 0; g < 8; ++g) jg[g] = 0;  // cum_0 = 0 <= every slot
+#pragma unroll
+        for (uint32_t step = 128; step > 0; step >>= 1) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const uint32_t t = jg[g] + step;
+                if (t < k_total && (plist[t] >> 8) <= 512 * uint32_t(g) + first) jg[g] = t;
             }
-            reinterpret_cast<uint32_t*>(slot_sym)[i0 / 4] = word;
+        }
+        const uint32_t slot_base = static_cast<uint32_t>(__cvta_generic_to_shared(slot_sym));
+#pragma unroll 1
+        for (uint32_t g = 0; g < 8; ++g) {
+            const uint32_t p0 = 512 * g + first;
+            uint32_t j = jg[0];
+#pragma unroll
+            for (int k = 1; k < 8; ++k) j = g == uint32_t(k) ? jg[k] : j;
+            uint32_t cur = plist[j] & 0xFFu;
+            uint32_t next_cum = j + 1 < k_total ? (plist[j + 1] >> 8) : kM;
+            uint32_t wq[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t i0 = p0 + 4 * q;
+                uint32_t word;
+                if (next_cum > i0 + 3) {
+                    word = cur * 0x01010101u;
+                } else {
+                    word = 0;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        while (next_cum <= i0 + b) {
+                            ++j;
+                            cur = plist[j] & 0xFFu;
+                            next_cum = j + 1 < k_total ? (plist[j + 1] >> 8) : kM;
+                        }
+                        word |= cur << (8 * b);
+                    }
+                }
+                wq[q] = word;
+            }
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(slot_base + p0), "r"(wq[0]), "r"(wq[1]),
+                         "r"(wq[2]), "r"(wq[3])
+                         : "memory");
         }
     }
     __syncwarp();
