@@ -149,3 +149,93 @@ def test_same_tensor_into_separate_buffers_at_once():
     import torch
 
     assert all(torch.equal(j.out, x) for j in jobs)
+
+
+def test_round_trips_through_host_buffers_overlapped_on_three_streams():
+    """Steps of input up, compress, container down at its exact size,
+    container up, decompress, output down, run as a two-slot pipeline on
+    upload, kernel and download streams (the schedule of the benchmark's
+    end-to-end figure), with a different tensor every step so that a buffer
+    reused too early would show: every container equals the oracle's and
+    every output the input."""
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+
+    steps, S, n = 6, 2, 5 * CH + 123
+    inputs = [synth.normal_bf16(n, 0.01 * (1 + k), 13, 40 + k) for k in range(steps)]
+    want = [oracle.compress(b) for b in inputs]
+    cap = uz.uzip_max_compressed_size(gu.BF16, n)
+    h_in = [torch.from_numpy(b.view(np.int16)).pin_memory() for b in inputs]
+    h_comp = [torch.empty(cap, dtype=torch.uint8).pin_memory() for _ in range(S)]
+    h_out = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(steps)]
+    h_size = torch.zeros(S, dtype=torch.int64).pin_memory()
+    got = [None] * steps
+    d_in = [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(S)]
+    d_comp = [torch.empty(cap, dtype=torch.uint8, device="cuda") for _ in range(S)]
+    d_size = [torch.zeros((), dtype=torch.int64, device="cuda") for _ in range(S)]
+    d_comp2 = [torch.empty(cap, dtype=torch.uint8, device="cuda") for _ in range(S)]
+    d_out = [torch.empty(n, dtype=torch.int16, device="cuda") for _ in range(S)]
+    d_status = [torch.full((), -1, dtype=torch.int32, device="cuda") for _ in range(S)]
+    up, ks, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = [{k: torch.cuda.Event() for k in ("comp", "cdn", "cup", "dec", "odn", "in")} for _ in range(S)]
+    tb = [0] * S
+    statuses = []
+    for k in range(steps + 1):
+        if k < steps:  # input k up, compress k
+            b, e = k % S, ev[k % S]
+            if k >= S:
+                up.wait_event(e["comp"])
+            with torch.cuda.stream(up):
+                d_in[b].copy_(h_in[k], non_blocking=True)
+            e["in"].record(up)
+            ks.wait_event(e["in"])
+            if k >= S:
+                ks.wait_event(e["cdn"])
+            with torch.cuda.stream(ks):
+                assert uz.uzip_compress(d_in[b].data_ptr(), gu.BF16, n, d_comp[b].data_ptr(), cap,
+                                        d_size[b].data_ptr(), ks.cuda_stream) == 0
+                h_size[b].copy_(d_size[b], non_blocking=True)
+            e["comp"].record(ks)
+        if k >= 1:  # container k - 1 up, decompress it
+            j = k - 1
+            b, e = j % S, ev[j % S]
+            up.wait_event(e["cdn"])
+            if j >= S:
+                up.wait_event(e["dec"])
+            with torch.cuda.stream(up):
+                d_comp2[b][:tb[b]].copy_(h_comp[b][:tb[b]], non_blocking=True)
+            e["cup"].record(up)
+            ks.wait_event(e["cup"])
+            if j >= S:
+                ks.wait_event(e["odn"])
+            with torch.cuda.stream(ks):
+                assert uz.uzip_decompress(d_comp2[b].data_ptr(), tb[b], d_out[b].data_ptr(), gu.BF16, n,
+                                          d_status[b].data_ptr(), ks.cuda_stream) == 0
+            e["dec"].record(ks)
+        if k < steps:  # the host reads size k; container k down
+            b, e = k % S, ev[k % S]
+            e["comp"].synchronize()
+            tb[b] = int(h_size[b])
+            down.wait_event(e["comp"])
+            if k >= S:
+                down.wait_event(e["cup"])
+            with torch.cuda.stream(down):
+                h_comp[b][:tb[b]].copy_(d_comp[b][:tb[b]], non_blocking=True)
+            e["cdn"].record(down)
+            e["cdn"].synchronize()  # keep a copy of container k for the oracle check
+            got[k] = h_comp[b][:tb[b]].numpy().copy()
+        if k >= 1:  # output k - 1 down
+            j = k - 1
+            b, e = j % S, ev[j % S]
+            down.wait_event(e["dec"])
+            with torch.cuda.stream(down):
+                h_out[j].copy_(d_out[b], non_blocking=True)
+            e["odn"].record(down)
+            e["odn"].synchronize()
+            statuses.append(int(d_status[b].item()))
+    torch.cuda.synchronize()
+    assert statuses == [0] * steps
+    for k in range(steps):
+        assert got[k].size == want[k].size and np.array_equal(got[k], want[k]), k
+        assert np.array_equal(h_out[k].numpy().view(np.uint16), inputs[k]), k
