@@ -147,3 +147,49 @@ def test_pipeline_send_sized(code):
         want = oracle.compress(m, code, mode=mode)
         assert int(sizes[k]) == want.size
         assert np.array_equal(hb[k % 2].numpy()[: want.size], want)
+
+
+def _msgs_of(code):
+    CH = 65536
+    if code == gu.BF16:
+        msgs = [synth.normal_bf16(n, 0.02, 8, 30 + t) for t, n in enumerate((5 * CH + 77, 2 * CH, CH + 1))]
+        rnd = np.random.default_rng(31).integers(0, 1 << 16, 2 * CH + 9, dtype=np.uint16)
+    elif code == gu.FP32:
+        msgs = [synth.normal_fp32(n, 0.02, tensor=30 + t) for t, n in enumerate((5 * CH + 77, 2 * CH, CH + 1))]
+        rnd = np.random.default_rng(31).integers(0, 1 << 32, 2 * CH + 9, dtype=np.uint64).astype(np.uint32)
+    else:
+        msgs = [_normal(code, n, tensor=30 + t) for t, n in enumerate((5 * CH + 77, 2 * CH, CH + 1))]
+        rnd = _random_bits(code, 2 * CH + 9, 31)
+    return msgs + [rnd]  # the last one's chunks are stored RAW
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("code", [gu.BF16, gu.FP32] + NEW)
+def test_pipeline_coded_messages_every_format_and_mode(code, mode):
+    """Coded containers (no whole-message RAW) of every element format through
+    every pipeline mode, including the streamed one, whose early copies of
+    finished remainder and stream runs follow each format's plane layout;
+    every container equals the oracle's."""
+    import torch
+
+    import lossless_float_tensor_gb300 as uz
+
+    msgs = _msgs_of(code)
+    d_msgs = [gu.to_device(m) for m in msgs]
+    largest = max(m.size for m in msgs)
+    cap = uz.uzip_max_compressed_size(code, largest)
+    banks = [torch.empty(cap, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    hcap = cap + 16 * (-(-largest // 65536))  # the streamed mode's progress words
+    hb = [torch.zeros(hcap, dtype=torch.uint8).pin_memory() for _ in msgs]
+    sizes = torch.zeros(len(msgs), dtype=torch.int64).pin_memory()
+    s0, s1 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    st = uz.uzip_pipeline_send_ex(code, [t.data_ptr() for t in d_msgs], [m.size for m in msgs],
+                                  [b.data_ptr() for b in banks], cap, [h.data_ptr() for h in hb], hcap,
+                                  sizes.data_ptr(), mode, 0, s0.cuda_stream, s1.cuda_stream)
+    assert st == 0, uz.uzip_status_string(st)
+    torch.cuda.synchronize()
+    for k, m in enumerate(msgs):
+        want = oracle.compress(m, code)
+        assert int(sizes[k]) == want.size, k
+        assert np.array_equal(hb[k].numpy()[: want.size], want), k
